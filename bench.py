@@ -1,0 +1,377 @@
+#!/usr/bin/env python
+"""Benchmark: exact attention forward + backward on GB300 through the C ABI.
+
+One step = fa_fwd + the three backward stages (preprocess, main, dQ convert) over one
+batch of seeded synthetic input already resident in HBM.  Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long_causal]
+    python bench.py --impl reference ...   # the CPU fp64 oracle on a bounded sample
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas: the
+(batch, head) units are independent, so there is no collective on the data path); the
+timed region is bracketed by barriers and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from exact_io_aware_28_gb300 import accounting as acc  # noqa: E402
+from exact_io_aware_28_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+# Kernels launched per step by the library (fwd, preprocess, main, dQ convert).
+KERNELS_PER_STEP = {"bf16": 4, "fp32": 4}
+
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clock sampling
+
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
+        if self.uuid:
+            mine = [r for r in rows if self.uuid in r[0]]
+            rows = mine or rows
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        under_load = [s for s in sm if mx and s > 0.3 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(under_load) if under_load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_head_seconds(x, head) -> float:
+    """Run the oracle's forward and backward on one (b, h) head; return wall seconds."""
+    import oracle
+    b, h = head
+    q, k, v, do = (t[b, h].to(torch.float64).numpy() for t in (x.q, x.k, x.v, x.do))
+    bm = None if x.blockmask is None else x.blockmask.numpy()
+    kl = None if x.kv_len is None else int(x.kv_len[b])
+    keep = oracle.keep_mask(q.shape[0], x.causal, bm, kl)
+    t0 = time.perf_counter()
+    oracle.forward_head(q, k, v, x.scale, keep)
+    oracle.backward_head(q, k, v, do, x.scale, keep)
+    return time.perf_counter() - t0
+
+
+def head_flops(w: W.Workload, x) -> float:
+    bm = None if x.blockmask is None else x.blockmask.numpy()
+    return acc.flops(1, 1, w.N, w.d, w.causal, bm)["fwd_bwd"]
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w: W.Workload, x_cpu) -> dict:
+    secs = oracle_head_seconds(x_cpu, (0, 0))
+    return {"value": head_flops(w, x_cpu) / secs / 1e12, "unit": UNIT, "cores": cpu_cores(),
+            "kind": "oracle",
+            "sample": f"one (batch, head) of {w.describe()}: fp64 NumPy forward + backward, "
+                      f"{secs:.1f} s; FLOPs by the same convention as the GPU figure"}
+
+
+def run_reference(args, world, rank):
+    """The CPU fp64 oracle as it stands: one (batch, head) of the workload per step."""
+    if rank != 0:
+        return
+    w = W.WORKLOADS[args.workload]
+    x = W.make_inputs(w, seed=0)
+    small = W.make_inputs(W.custom("warm", 1, 1, 256, w.d, w.dtype, causal=w.causal), seed=1)
+    for _ in range(args.warmup):
+        oracle_head_seconds(small, (0, 0))
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    times = [oracle_head_seconds(x, heads[i % len(heads)]) for i in range(args.steps)]
+    mean = sum(times) / len(times)
+    value = head_flops(w, x) / mean / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.describe(), "sample": "one (batch, head) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"one (batch, head) of {w.describe()} per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, world, rank, local):
+    from exact_io_aware_28_gb300 import fa
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.WORKLOADS[args.workload]
+    x_cpu = W.make_inputs(w, seed=0)
+    x = W.make_inputs(w, seed=0)
+    x.q, x.k, x.v, x.do = (t.to(dev) for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.do))
+    if x.kv_len is not None:
+        x.kv_len = x.kv_len.to(dev)
+    if x.blockmask is not None:
+        x.blockmask = x.blockmask.to(dev)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    o = torch.empty_like(x.q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(x.q), torch.empty_like(x.q), torch.empty_like(x.q)
+    ws = fa.alloc_workspace(B, H, N, d, dev)
+    bm_np = None if x_cpu.blockmask is None else x_cpu.blockmask.numpy()
+    fl = acc.flops(B, H, N, d, w.causal, bm_np)
+    elem = 2 if w.dtype == "bf16" else 4
+    in_bytes = 4 * B * H * N * d * elem
+    flush = in_bytes < 2 * L2_BYTES
+    scratch = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        fa.fa_fwd(x.q, x.k, x.v, o, lse, x.causal, x.blockmask, x.kv_len, x.scale, stream)
+        if ev:
+            ev[1].record(stream)
+        fa.fa_bwd_preprocess(o, x.do, ws, stream)
+        if ev:
+            ev[2].record(stream)
+        fa.fa_bwd_main(x.q, x.k, x.v, lse, x.do, dq, dk, dv, ws, x.causal, x.blockmask,
+                       x.kv_len, x.scale, stream)
+        if ev:
+            ev[3].record(stream)
+        fa.fa_bwd_dq_convert(dq, ws, x.scale, stream)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_error() != fa.FA_OK:
+        raise RuntimeError("device error word set during warm-up")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        if flush:
+            scratch.fill_(i & 0xFF)
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    if fa.fa_device_error() != fa.FA_OK:
+        raise RuntimeError("device error word set during the timed region")
+
+    phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
+                      for i in range(args.steps)])  # ms: fwd, preprocess, main, convert
+    step_ms = phase.sum(axis=1)
+    ms_per_step = float(step_ms.mean()) if flush else t_start.elapsed_time(t_end) / args.steps
+    ms_per_step = max_over_ranks(ms_per_step, world)
+    value = world * fl["fwd_bwd"] / (ms_per_step * 1e-3) / 1e12
+    pk = peaks()
+    mean_phase = phase.mean(axis=0)
+    fwd_tf = fl["fwd"] / (mean_phase[0] * 1e-3) / 1e12
+    bwd_ms = mean_phase[1:].sum()
+    bwd_tf = fl["bwd"] / (bwd_ms * 1e-3) / 1e12
+    main_tf = fl["bwd"] / (mean_phase[2] * 1e-3) / 1e12
+    pre_gbs = acc.preprocess_bytes(B, H, N, d, elem) / (mean_phase[1] * 1e-3) / 1e9
+    conv_gbs = (acc.dq_convert_bytes(B, H, N, d, elem) / (mean_phase[3] * 1e-3) / 1e9
+                if w.dtype == "bf16" else None)
+    peak_t = pk["bf16_tflops_sustained"]
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            traffic = json.load(open(tr_path)).get(args.workload, {}).get("bwd_main")
+        except ValueError:
+            traffic = None
+    roofline = {"kernel": "bwd main (dK, dV, dQ partials)", "bound": "tensor",
+                "achieved": main_tf, "peak": peak_t, "unit": "TFLOP/s",
+                "frac": main_tf / peak_t, "traffic": traffic,
+                "peak_kind": f"{pk['source']} bf16 dense, sustained"}
+
+    # e2e: the same step through the public API with host buffers and copies timed.
+    pin = [t.pin_memory() for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.do)]
+    outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    e2e_steps = max(1, min(args.steps, 5))
+    dev_in = (x.q, x.k, x.v, x.do)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for hsrc, ddst in zip(pin, dev_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        for hdst, dsrc in zip(outs, (o, lse, dq, dk, dv)):
+            hdst.copy_(dsrc, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    e2e = {"value": world * fl["fwd_bwd"] / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, x_cpu)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.describe(), "B": B, "H": H, "N": N, "d": d,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "flushed between steps (256 MiB write)" if flush
+                       else f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q, K, V, dO)",
+                       "flops_per_step": fl["fwd_bwd"]},
+            "pct_of_peak": value / world / peak_t,
+            "phases": {"fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "bwd_main_tflops": main_tf,
+                       "fwd_ms": mean_phase[0], "preprocess_ms": mean_phase[1],
+                       "bwd_main_ms": mean_phase[2], "dq_convert_ms": mean_phase[3],
+                       "preprocess_gbs": pre_gbs, "dq_convert_gbs": conv_gbs,
+                       "hbm_peak_gbs": pk["hbm_gbs"]},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP[w.dtype] * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line, default=float), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=W.ORDER, default="long_causal")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

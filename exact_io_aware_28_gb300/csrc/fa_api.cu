@@ -1,0 +1,215 @@
+// C-ABI boundary of libfa_gb300.so: argument validation, workspace carving and kernel
+// dispatch.  Every entry point validates on the host before launching anything; no entry
+// point allocates device memory or synchronises the stream (fa_device_error excepted).
+#include <math.h>
+#include <stdint.h>
+
+#include "fa_internal.cuh"
+
+namespace fa {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];      // 0 = not yet queried
+int* g_err_ptr[kMaxDevices];      // device address of the error word, per device
+}  // namespace
+
+// Device error word: a kernel whose bounded wait runs out stores FA_ERR_TIMEOUT here.
+static __device__ int g_device_error;
+
+int sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+int* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(ptr);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+fa_status check_shape(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * H > 65535) return FA_ERR_UNSUPPORTED;
+  if (N > (1 << 24)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: shape not supported";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA runtime error";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded device wait ran out";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d) != FA_OK) return 0;
+  const size_t rows = (size_t)B * H * N;
+  return round_up(rows * sizeof(float), 256) + rows * (size_t)d * sizeof(float);
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, int causal,
+                 const uint8_t* blockmask, const int32_t* kv_len,
+                 float scale, fa_dtype dtype, void* stream) {
+  fa_status st = check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  int* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_fwd_simt(p, dtype, q, k, v, o, lse, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+namespace {
+
+struct Workspace {
+  float* Dsum;
+  float* dq_acc;
+};
+
+Workspace carve(void* workspace, int B, int H, int N) {
+  const size_t rows = (size_t)B * H * N;
+  Workspace w;
+  w.Dsum = static_cast<float*>(workspace);
+  w.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                      fa::round_up(rows * sizeof(float), 256));
+  return w;
+}
+
+fa_status check_common(int B, int H, int N, int d, fa_dtype dtype, void* workspace,
+                       size_t workspace_bytes) {
+  fa_status st = fa::check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+bool bad_ptr(const void* p) { return !p || !fa::aligned16(p); }
+
+fa_status check_masks_scale(const int32_t* kv_len, const float* lse, float scale) {
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+fa_status to_status(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+fa_status fa_bwd_preprocess(const void* o, const void* dO, int B, int H, int N, int d,
+                            fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  fa_status st = check_common(B, H, N, d, dtype, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  if (bad_ptr(o) || bad_ptr(dO)) return FA_ERR_INVALID_ARG;
+  Problem p{B, H, N, d, 0, nullptr, nullptr, 1.f, nullptr};
+  Workspace w = carve(workspace, B, H, N);
+  return to_status(launch_bwd_preprocess(p, dtype, o, dO, w.Dsum,
+                                         dtype == FA_BF16 ? w.dq_acc : nullptr,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* lse,
+                      const void* dO, void* dq, void* dk, void* dv,
+                      int B, int H, int N, int d, int causal,
+                      const uint8_t* blockmask, const int32_t* kv_len,
+                      float scale, fa_dtype dtype,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = check_common(B, H, N, d, dtype, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  if (bad_ptr(q) || bad_ptr(k) || bad_ptr(v) || bad_ptr(dO) || bad_ptr(dk) || bad_ptr(dv))
+    return FA_ERR_INVALID_ARG;
+  if (dtype == FA_FP32 && bad_ptr(dq)) return FA_ERR_INVALID_ARG;
+  st = check_masks_scale(kv_len, lse, scale);
+  if (st != FA_OK) return st;
+  int* err = fa::error_word();
+  if (!err) return FA_ERR_CUDA;
+  Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err};
+  Workspace w = carve(workspace, B, H, N);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return to_status(launch_bwd_simt(p, dtype, q, k, v, lse, dO, w.Dsum, dq, dk, dv, s));
+}
+
+fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, fa_dtype dtype,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = check_common(B, H, N, d, dtype, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  if (bad_ptr(dq)) return FA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_FP32) return FA_OK;
+  (void)stream;
+  return FA_OK;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, int causal,
+                 const uint8_t* blockmask, const int32_t* kv_len,
+                 float scale, fa_dtype dtype,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = check_common(B, H, N, d, dtype, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  if (bad_ptr(q) || bad_ptr(k) || bad_ptr(v) || bad_ptr(o) || bad_ptr(dO) || bad_ptr(dq) ||
+      bad_ptr(dk) || bad_ptr(dv))
+    return FA_ERR_INVALID_ARG;
+  st = check_masks_scale(kv_len, lse, scale);
+  if (st != FA_OK) return st;
+  st = fa_bwd_preprocess(o, dO, B, H, N, d, dtype, workspace, workspace_bytes, stream);
+  if (st != FA_OK) return st;
+  st = fa_bwd_main(q, k, v, lse, dO, dq, dk, dv, B, H, N, d, causal, blockmask, kv_len, scale,
+                   dtype, workspace, workspace_bytes, stream);
+  if (st != FA_OK) return st;
+  return fa_bwd_dq_convert(dq, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  int host = 0;
+  if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  return host == 0 ? FA_OK : static_cast<fa_status>(host);
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// Internal declarations shared by the translation units of libfa_gb300.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "fa.h"
+
+namespace fa {
+
+constexpr int kMaskBlock = FA_MASK_BLOCK;
+
+// Problem description handed from the C-ABI layer to the launchers.  Pointers are
+// device pointers; element pointers are typed by the launcher.
+struct Problem {
+  int B, H, N, d;
+  int causal;
+  const uint8_t* blockmask;  // [nb, nb] or nullptr
+  const int32_t* kv_len;     // [B] or nullptr
+  float scale;
+  int* err;                  // device error word
+};
+
+// Device error codes written into the error word (match fa_status).
+constexpr int kErrTimeout = FA_ERR_TIMEOUT;
+
+// Launchers.  Each returns cudaSuccess or the launch error.
+cudaError_t launch_fwd_simt(const Problem& p, fa_dtype dt, const void* q, const void* k,
+                            const void* v, void* o, float* lse, cudaStream_t s);
+cudaError_t launch_bwd_simt(const Problem& p, fa_dtype dt, const void* q, const void* k,
+                            const void* v, const float* lse, const void* dO, const float* D,
+                            void* dq, void* dk, void* dv, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const Problem& p, fa_dtype dt, const void* o, const void* dO,
+                                  float* D, float* dq_acc, cudaStream_t s);
+cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, void* dq, cudaStream_t s);
+cudaError_t launch_fwd_sm103(const Problem& p, const void* q, const void* k, const void* v,
+                             void* o, float* lse, cudaStream_t s);
+cudaError_t launch_bwd_sm103(const Problem& p, const void* q, const void* k, const void* v,
+                             const float* lse, const void* dO, const float* D, float* dq_acc,
+                             void* dk, void* dv, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace fa

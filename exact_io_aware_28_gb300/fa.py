@@ -1,0 +1,187 @@
+"""ctypes binding of libfa_gb300.so (names as in include/fa.h).
+
+Argument marshalling only: every step of the attention path runs in the library's
+CUDA kernels.  torch supplies device memory and the current stream.  If the library
+has not been built, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_BF16, FA_FP32 = 0, 1
+
+# Every symbol include/fa.h declares.
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_preprocess", "fa_bwd_main",
+           "fa_bwd_dq_convert", "fa_status_string", "fa_device_error")
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)}")
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m exact_io_aware_28_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, F, I, P]
+    lib.fa_fwd.restype = I
+    lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, F, I, P, S, P]
+    lib.fa_bwd.restype = I
+    lib.fa_bwd_preprocess.argtypes = [P, P, I, I, I, I, I, P, S, P]
+    lib.fa_bwd_preprocess.restype = I
+    lib.fa_bwd_main.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, F, I, P, S, P]
+    lib.fa_bwd_main.restype = I
+    lib.fa_bwd_dq_convert.argtypes = [P, I, I, I, I, F, I, P, S, P]
+    lib.fa_bwd_dq_convert.restype = I
+    lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
+    lib.fa_bwd_workspace_bytes.restype = S
+    lib.fa_status_string.argtypes = [I]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_device_error.argtypes = [P]
+    lib.fa_device_error.restype = I
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+def _check_dense(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B, H, N, d]")
+
+
+def fa_status_string(status: int) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_device_error(stream=None) -> int:
+    return int(load().fa_device_error(_stream(stream)))
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool = False, blockmask=None, kv_len=None,
+           scale: Optional[float] = None, stream=None) -> None:
+    """O and lse for [B, H, N, d] tensors q, k, v (outputs o, lse preallocated)."""
+    _check_dense(q, k, v, o, lse, blockmask, kv_len)
+    B, H, N, d = q.shape
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    st = load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(causal),
+                       _ptr(blockmask), _ptr(kv_len), scale, _dtype_code(q), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+
+
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, causal: bool = False, blockmask=None,
+           kv_len=None, scale: Optional[float] = None, stream=None) -> None:
+    """dq, dk, dv (preallocated) for the upstream gradient ``do``."""
+    _check_dense(q, k, v, o, lse, do, dq, dk, dv, blockmask, kv_len)
+    B, H, N, d = q.shape
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                       _ptr(dk), _ptr(dv), B, H, N, d, int(causal), _ptr(blockmask),
+                       _ptr(kv_len), scale, _dtype_code(q), _ptr(workspace), ws_bytes,
+                       _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+
+
+def fa_bwd_preprocess(o, do, workspace, stream=None) -> None:
+    B, H, N, d = o.shape
+    st = load().fa_bwd_preprocess(_ptr(o), _ptr(do), B, H, N, d, _dtype_code(o),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_preprocess")
+
+
+def fa_bwd_main(q, k, v, lse, do, dq, dk, dv, workspace, causal=False, blockmask=None,
+                kv_len=None, scale=None, stream=None) -> None:
+    _check_dense(q, k, v, lse, do, dq, dk, dv, blockmask, kv_len)
+    B, H, N, d = q.shape
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    st = load().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                            _ptr(dv), B, H, N, d, int(causal), _ptr(blockmask), _ptr(kv_len),
+                            scale, _dtype_code(q), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_main")
+
+
+def fa_bwd_dq_convert(dq, workspace, scale=None, stream=None) -> None:
+    B, H, N, d = dq.shape
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    st = load().fa_bwd_dq_convert(_ptr(dq), B, H, N, d, scale, _dtype_code(dq), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_dq_convert")
+
+
+# ----------------------------------------------------------- allocating helpers
+
+def alloc_workspace(B: int, H: int, N: int, d: int, device="cuda") -> torch.Tensor:
+    n = fa_bwd_workspace_bytes(B, H, N, d)
+    if n == 0:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_bwd_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def forward(q, k, v, causal=False, blockmask=None, kv_len=None, scale=None, stream=None):
+    """Allocate O and lse with torch and run fa_fwd.  Returns (o, lse)."""
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, causal, blockmask, kv_len, scale, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, causal=False, blockmask=None, kv_len=None, scale=None,
+             workspace=None, stream=None):
+    """Allocate dQ, dK, dV (and the workspace unless given) and run fa_bwd."""
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, N, d, q.device)
+    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, causal, blockmask, kv_len, scale, stream)
+    return dq, dk, dv

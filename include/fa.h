@@ -1,0 +1,144 @@
+/*
+ * fa.h -- C ABI of the exact IO-aware attention library (libfa_gb300.so).
+ *
+ * What it computes (FlashAttention pages):
+ *   forward  -- "How FlashAttention works for training" (aivaro.ru answer 474),
+ *               sections 1 and 2.1: O = softmax(Q K^T * scale) V, computed tile by
+ *               tile with a running row maximum and row sum (online softmax, FlashAttention
+ *               reading guide arXiv 2205.14135, "Method", steps 1-4), never writing
+ *               the N x N score or probability matrix to memory.  Besides O it writes the
+ *               per-row logsumexp, the one statistic the backward needs (course week 13,
+ *               step 2).
+ *   backward -- answer page section 3.1 and course week 13, step 2: S and P are
+ *               recomputed block by block from Q, K and the saved logsumexp; with
+ *               D = rowsum(dO o O) the gradients are the chain-rule ones
+ *               dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = scale dS K,
+ *               dK = scale dS^T Q.
+ *   masks    -- causal (course week 13, step 2: key j visible to query i iff j <= i, tiles
+ *               wholly above the diagonal are skipped) and block-sparse (reading guide,
+ *               "Extension: block-sparse FlashAttention": a 0/1 mask over blocks; zero
+ *               blocks are skipped).  Per-sequence key padding masks key j >= kv_len[b].
+ *
+ * Layout: Q, K, V, O, dO, dQ, dK, dV are dense row-major [B, H, N, d] (d innermost,
+ * then N, then H, then B), element type given by `dtype`.  lse and the D row sums are
+ * fp32 [B, H, N].  Only d = 64 and d = 128 are supported.
+ *
+ * Memory: every pointer (tensors, kv_len, blockmask, workspace) is a DEVICE pointer owned
+ * by the caller; the library allocates no device memory per call.  Tensor pointers must be
+ * 16-byte aligned.  Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ * NULL is the legacy default stream): outputs are valid once the stream has synchronised.
+ *
+ * Errors: arguments are validated on the host before any launch; a failed check returns
+ * FA_ERR_INVALID_ARG (bad pointer, size, alignment, dtype, workspace) or FA_ERR_UNSUPPORTED
+ * (a shape the kernels do not cover) and launches nothing.  A launch failure reported by the
+ * CUDA runtime returns FA_ERR_CUDA.  Device-side faults surface at the caller's next
+ * synchronisation.  A bounded wait inside a kernel that runs out records FA_ERR_TIMEOUT in
+ * the library's device error word, readable with fa_device_error().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_UNSUPPORTED = 2,
+  FA_ERR_CUDA = 3,
+  FA_ERR_TIMEOUT = 4
+} fa_status;
+
+typedef enum {
+  FA_BF16 = 0, /* bf16 tensors; tcgen05 tensor-core kernels, fp32 accumulation */
+  FA_FP32 = 1  /* fp32 tensors; fp32 CUDA-core kernels                          */
+} fa_dtype;
+
+/* Block-mask granularity: one mask entry covers 128 query rows x 128 key columns. */
+#define FA_MASK_BLOCK 128
+
+/*
+ * Forward pass.
+ *   q, k, v   in : [B, H, N, d] of `dtype`.
+ *   o         out: [B, H, N, d] of `dtype`, O = softmax(scale Q K^T + mask) V.
+ *   lse       out: fp32 [B, H, N], natural-log logsumexp of each masked, scaled score row;
+ *                  -inf for a row that sees no key (its O row is 0).
+ *   causal       : nonzero = key j is visible to query i only when j <= i (top-left aligned).
+ *   blockmask    : NULL, or device uint8 [nb, nb] with nb = ceil(N / 128), row-major, shared by
+ *                  every (b, h); entry [I][J] = 0 hides keys 128J..128J+127 from queries
+ *                  128I..128I+127 (the block is skipped).
+ *   kv_len       : NULL, or device int32 [B]; keys j >= kv_len[b] are hidden from every query of
+ *                  sequence b.  Values are clamped to [0, N] on the device.
+ *   scale        : multiplier of Q K^T, normally 1/sqrt(d); must be finite.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, int causal,
+                 const uint8_t* blockmask, const int32_t* kv_len,
+                 float scale, fa_dtype dtype, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: the fp32 row sums D [B, H, N] followed (at a
+ * 256-byte aligned offset) by the fp32 dQ accumulator [B, H, N, d].  Returns 0 when the
+ * sizes are invalid.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass for the loss gradient dO = dL/dO.
+ *   q, k, v, o   in : as given to / returned by fa_fwd (same masks, same scale).
+ *   lse          in : fp32 [B, H, N] as returned by fa_fwd.
+ *   dO           in : [B, H, N, d] of `dtype`.
+ *   dq, dk, dv   out: [B, H, N, d] of `dtype`.
+ *   workspace       : device buffer of at least fa_bwd_workspace_bytes(B, H, N, d) bytes,
+ *                     256-byte aligned; its contents on entry do not matter.
+ * Rows that see no key (lse = -inf) contribute nothing to any gradient.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dO, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, int causal,
+                 const uint8_t* blockmask, const int32_t* kv_len,
+                 float scale, fa_dtype dtype,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The three stages fa_bwd runs, in order, on `stream` (same arguments and workspace; the
+ * workspace must not be reused by another call until the last stage has run):
+ *   fa_bwd_preprocess  -- D = rowsum(dO o O) (fp32, into the workspace) and, for bf16,
+ *                         zeroes the fp32 dQ accumulator;
+ *   fa_bwd_main        -- recomputes S and P block by block and forms dK and dV (written
+ *                         to dk, dv) and dQ (bf16: summed into the fp32 accumulator;
+ *                         fp32: written to dq directly);
+ *   fa_bwd_dq_convert  -- bf16: dq = bf16(scale * accumulator); fp32: nothing to do.
+ * They exist so that each kernel can be timed on its own; fa_bwd is their composition.
+ */
+fa_status fa_bwd_preprocess(const void* o, const void* dO, int B, int H, int N, int d,
+                            fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                            void* stream);
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* lse,
+                      const void* dO, void* dq, void* dk, void* dv,
+                      int B, int H, int N, int d, int causal,
+                      const uint8_t* blockmask, const int32_t* kv_len,
+                      float scale, fa_dtype dtype,
+                      void* workspace, size_t workspace_bytes, void* stream);
+fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, fa_dtype dtype,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the current
+ * device: FA_OK if no kernel recorded an error, FA_ERR_TIMEOUT if a bounded wait ran out,
+ * FA_ERR_CUDA if the synchronisation itself failed.
+ */
+fa_status fa_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

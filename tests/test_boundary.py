@@ -1,0 +1,112 @@
+"""The C-ABI library: it loads, exports what include/fa.h declares, and rejects bad
+arguments on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_io_aware_28_gb300 import fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+pytestmark = pytest.mark.skipif(not os.path.exists(fa.LIB_PATH),
+                                reason="libfa_gb300.so not built")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(fa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(fa.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    for code in range(5):
+        assert fa.fa_status_string(code).startswith("FA_")
+    assert "UNKNOWN" in fa.fa_status_string(99)
+
+
+def test_workspace_bytes():
+    B, H, N, d = 1, 32, 16384, 128
+    rows = B * H * N
+    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == rows * 4 + rows * d * 4
+    assert fa.fa_bwd_workspace_bytes(1, 1, 7, 64) == 256 + 7 * 64 * 4
+    assert fa.fa_bwd_workspace_bytes(1, 1, 0, 64) == 0
+    assert fa.fa_bwd_workspace_bytes(1, 1, 8, 96) == 0
+
+
+A = 0x10000  # a fake, 16-byte aligned address: never dereferenced on the host
+
+
+def fwd(**kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=128, d=64, causal=0, bm=None,
+                kv=None, scale=0.125, dtype=fa.FA_BF16)
+    args.update(kw)
+    lib = fa.load()
+    return lib.fa_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                      args["H"], args["N"], args["d"], args["causal"], args["bm"], args["kv"],
+                      args["scale"], args["dtype"], None)
+
+
+def bwd(**kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, do=A, dq=A, dk=A, dv=A, B=1, H=1, N=128, d=64,
+                causal=0, bm=None, kv=None, scale=0.125, dtype=fa.FA_BF16, ws=A,
+                wsb=1 << 30)
+    args.update(kw)
+    lib = fa.load()
+    return lib.fa_bwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["do"],
+                      args["dq"], args["dk"], args["dv"], args["B"], args["H"], args["N"],
+                      args["d"], args["causal"], args["bm"], args["kv"], args["scale"],
+                      args["dtype"], args["ws"], args["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"q": None}, fa.FA_ERR_INVALID_ARG),
+    ({"lse": None}, fa.FA_ERR_INVALID_ARG),
+    ({"N": 0}, fa.FA_ERR_INVALID_ARG),
+    ({"B": 0}, fa.FA_ERR_INVALID_ARG),
+    ({"d": 96}, fa.FA_ERR_UNSUPPORTED),
+    ({"d": 256}, fa.FA_ERR_UNSUPPORTED),
+    ({"k": A + 8}, fa.FA_ERR_INVALID_ARG),
+    ({"o": A + 2}, fa.FA_ERR_INVALID_ARG),
+    ({"lse": A + 1}, fa.FA_ERR_INVALID_ARG),
+    ({"kv": A + 2}, fa.FA_ERR_INVALID_ARG),
+    ({"dtype": 7}, fa.FA_ERR_INVALID_ARG),
+    ({"scale": float("nan")}, fa.FA_ERR_INVALID_ARG),
+    ({"scale": float("inf")}, fa.FA_ERR_INVALID_ARG),
+    ({"B": 300, "H": 300}, fa.FA_ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_bad_arguments(kw, code):
+    assert fwd(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"do": None}, fa.FA_ERR_INVALID_ARG),
+    ({"ws": None}, fa.FA_ERR_INVALID_ARG),
+    ({"dq": A + 4}, fa.FA_ERR_INVALID_ARG),
+    ({"ws": A + 16}, fa.FA_ERR_INVALID_ARG),
+    ({"wsb": 1000}, fa.FA_ERR_INVALID_ARG),
+    ({"d": 32}, fa.FA_ERR_UNSUPPORTED),
+    ({"N": -5}, fa.FA_ERR_INVALID_ARG),
+    ({"dtype": -1}, fa.FA_ERR_INVALID_ARG),
+])
+def test_bwd_rejects_bad_arguments(kw, code):
+    assert bwd(**kw) == code
+
+
+def test_binding_refuses_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(fa, "_lib", None)
+    monkeypatch.setattr(fa, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        fa.load()
