@@ -87,12 +87,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return FA_ERR_INVALID_ARG;
   if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_INVALID_ARG;
-  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
   int* err = error_word();
   if (!err) return FA_ERR_CUDA;
   Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_fwd_simt(p, dtype, q, k, v, o, lse, s);
+  cudaError_t e = dtype == FA_BF16 ? launch_fwd_sm103(p, q, k, v, o, lse, s)
+                                   : launch_fwd_simt(p, dtype, q, k, v, o, lse, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -127,7 +128,7 @@ bool bad_ptr(const void* p) { return !p || !fa::aligned16(p); }
 fa_status check_masks_scale(const int32_t* kv_len, const float* lse, float scale) {
   if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0) return FA_ERR_INVALID_ARG;
-  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
   return FA_OK;
 }
 
@@ -174,7 +175,7 @@ fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, f
   fa_status st = check_common(B, H, N, d, dtype, workspace, workspace_bytes);
   if (st != FA_OK) return st;
   if (bad_ptr(dq)) return FA_ERR_INVALID_ARG;
-  if (!isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (dtype == FA_FP32) return FA_OK;
   (void)stream;
   return FA_OK;

@@ -1,0 +1,476 @@
+// Forward attention on sm_103a tensor cores (tcgen05 + TMA), bf16 in, fp32 accumulate.
+//
+// What it computes is the tiled forward with a running (max, sum) state: for each block
+// of 128 query rows and each block j of 128 keys, S_ij = Q_i K_j^T, the running row
+// maximum and row sum are updated and O_i is rescaled and accumulated with P_ij V_j
+// (FlashAttention reading guide, arXiv 2205.14135, "Method", steps 1-4; answer page
+// "How FlashAttention works for training", section 2.1).  O is kept unnormalised and
+// divided by the row sum once at the end (course week 13, step 2 keeps the unnormalised
+// accumulator and multiplies it by e^{m_old - m_new} on a new maximum); the only other
+// output is the per-row logsumexp.  Key blocks wholly above the causal diagonal and zero
+// blocks of the 128 x 128 block mask are never loaded or multiplied (course week 13,
+// step 2; reading guide, "Extension: block-sparse FlashAttention").
+//
+// GB300 mapping (one CTA = 256 query rows of one (batch, head) = two 128-row tiles):
+//   warp 0        TMA producer: Q0, Q1 once, then K_j, V_j through a ring of stages;
+//   warp 1        MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, O_t += P_t V_j with P
+//                 read from TMEM; issue order PV0(j), S0(j+1), PV1(j), S1(j+1) keeps the
+//                 tensor pipe busy while each softmax warpgroup works on its own tile;
+//   warp 2        tensor-memory allocation;
+//   warps 4-7     softmax for tile 0, warps 8-11 softmax for tile 1: one thread per row,
+//                 scores read with tcgen05.ld, exp2 with scale*log2(e) folded in, P written
+//                 back as bf16 over the first 64 columns of its own S region, O rescaled in
+//                 TMEM only when the running maximum grows by more than 2^8 (exact: the
+//                 final division uses the same reference maximum);
+//   epilogue      the softmax warps read O from TMEM, divide by the row sum and store bf16.
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [384,384+d).
+// Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and exits cleanly.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "fa_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBlk = 128;               // rows of a Q tile / keys of a K,V tile
+constexpr int kSub = 128 * 128;         // bytes of a [128 rows][64 bf16] 128B-swizzled subtile
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past a 256x growth
+constexpr int kThreads = 384;
+
+template <int D>
+struct Cfg {
+  static constexpr int NSUB = D / 64;
+  static constexpr int TILE = NSUB * kSub;
+  static constexpr int NSTAGE = D == 128 ? 4 : 8;
+  static constexpr int SMEM = 1024 + 2 * TILE + NSTAGE * TILE + 256;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int never;  // stays 0: waits that must not be cut short by an abort
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+struct Unit {
+  int bh, q0, L, nb;
+};
+
+// Does query tile t (rows q0 + 128t ...) of this unit need key block j?
+__device__ __forceinline__ bool need(const Problem& p, const Unit& u, int t, int j) {
+  const int r0 = u.q0 + t * kBlk;
+  if (r0 >= p.N) return false;
+  if (j * kBlk >= u.L) return false;
+  if (p.causal && j * kBlk > r0 + kBlk - 1) return false;
+  if (p.blockmask && !p.blockmask[(r0 / kBlk) * u.nb + j]) return false;
+  return true;
+}
+
+__device__ __forceinline__ int key_blocks(const Problem& p, const Unit& u) {
+  int jend = (u.L + kBlk - 1) / kBlk;
+  if (p.causal) {
+    const int last_row = min(u.q0 + 2 * kBlk, p.N) - 1;
+    jend = min(jend, last_row / kBlk + 1);
+  }
+  return jend;
+}
+
+__device__ __forceinline__ int next_any(const Problem& p, const Unit& u, int j, int jend) {
+  for (++j; j < jend; ++j)
+    if (need(p, u, 0, j) || need(p, u, 1, j)) return j;
+  return -1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                 const __grid_constant__ CUtensorMap mv, __nv_bfloat16* __restrict__ o,
+                 float* __restrict__ lse, Problem p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = base;                       // [2][TILE]
+  uint8_t* sKV = base + 2 * C::TILE;        // [NSTAGE][TILE]
+  Bars* bars = reinterpret_cast<Bars*>(sKV + C::NSTAGE * C::TILE);
+  volatile int* abort_flag = &bars->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // Work unit: heavy (late, causal) query blocks first.
+  const int nqb = (p.N + 2 * kBlk - 1) / (2 * kBlk);
+  const int bhs = p.B * p.H;
+  Unit u;
+  u.bh = blockIdx.x % bhs;
+  u.q0 = (nqb - 1 - static_cast<int>(blockIdx.x / bhs)) * 2 * kBlk;
+  {
+    int L = p.N;
+    if (p.kv_len) {
+      const int b = u.bh / p.H;
+      L = p.kv_len[b];
+      L = L < 0 ? 0 : (L > p.N ? p.N : L);
+    }
+    u.L = L;
+  }
+  u.nb = (p.N + kBlk - 1) / kBlk;
+  const int jend = key_blocks(p, u);
+
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], kBlk);
+      mbar_init(&bars->o_done[t], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    bars->never = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE);
+      for (int t = 0; t < 2; ++t)
+        for (int s = 0; s < C::NSUB; ++s)
+          tma_load_3d(sQ + t * C::TILE + s * kSub, &mq, &bars->q_full, 64 * s, u.q0 + t * kBlk,
+                      u.bh);
+      int stage = 0, round = 0;
+      bool ok = true;
+      for (int j = next_any(p, u, -1, jend); ok && j >= 0; j = next_any(p, u, j, jend)) {
+        for (int which = 0; which < 2 && ok; ++which) {
+          ok = mbar_wait(&bars->kv_empty[stage], (round & 1) ^ 1, abort_flag, p.err, kWaitNs);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars->kv_full[stage], C::TILE);
+          const CUtensorMap* m = which == 0 ? &mk : &mv;
+          for (int s = 0; s < C::NSUB; ++s)
+            tma_load_3d(sKV + stage * C::TILE + s * kSub, m, &bars->kv_full[stage], 64 * s,
+                        j * kBlk, u.bh);
+          if (++stage == C::NSTAGE) {
+            stage = 0;
+            ++round;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
+      int last[2] = {-1, -1};
+      for (int j = 0; j < jend; ++j)
+        for (int t = 0; t < 2; ++t)
+          if (need(p, u, t, j)) last[t] = j;
+      int cs = 0, cr = 0;           // ring position consumed
+      int npv[2] = {0, 0};
+      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, kWaitNs);
+      tc_fence_after();
+      auto issue_s = [&](int t, uint32_t kaddr) {
+        const uint32_t qaddr = sQa + t * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
+          mma_ss(tb + t * 128, sw128_desc(qaddr + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024),
+                 idS, kk > 0);
+        }
+        mma_commit(&bars->s_full[t]);
+      };
+      auto issue_pv = [&](int t, uint32_t vaddr) {
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ts(tb + 256 + t * 128, tb + t * 128 + 8 * kk,
+                 sw128_desc(vaddr + 2048 * kk, kSub, 1024), idO, (npv[t] > 0 || kk > 0) ? 1u : 0u);
+        ++npv[t];
+      };
+      auto wait_full = [&]() -> bool {
+        const bool r = mbar_wait(&bars->kv_full[cs], cr & 1, abort_flag, p.err, kWaitNs);
+        tc_fence_after();
+        return r;
+      };
+      auto advance = [&]() {
+        if (++cs == C::NSTAGE) {
+          cs = 0;
+          ++cr;
+        }
+      };
+      int j = next_any(p, u, -1, jend);
+      if (ok && j >= 0) {
+        ok = wait_full();
+        if (ok) {
+          const uint32_t kaddr = sKVa + cs * C::TILE;
+          for (int t = 0; t < 2; ++t)
+            if (need(p, u, t, j)) issue_s(t, kaddr);
+          mma_commit(&bars->kv_empty[cs]);
+          advance();
+        }
+      }
+      while (ok && j >= 0) {
+        const int jn = next_any(p, u, j, jend);
+        ok = wait_full();  // V_j
+        if (!ok) break;
+        const int vs = cs;
+        const uint32_t vaddr = sKVa + vs * C::TILE;
+        advance();
+        int ks = -1;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (need(p, u, t, j)) {
+            ok = mbar_wait(&bars->p_full[t], (npv[t] & 1), abort_flag, p.err, kWaitNs);
+            tc_fence_after();
+            if (!ok) break;
+            issue_pv(t, vaddr);
+            if (j == last[t]) mma_commit(&bars->o_done[t]);
+          }
+          if (t == 0) {
+            // K of the next key block follows V_j in the ring.
+            if (jn >= 0) {
+              ok = wait_full();
+              if (!ok) break;
+              ks = cs;
+              advance();
+              if (need(p, u, 0, jn)) issue_s(0, sKVa + ks * C::TILE);
+            }
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bars->kv_empty[vs]);
+        if (jn >= 0) {
+          if (need(p, u, 1, jn)) issue_s(1, sKVa + ks * C::TILE);
+          mma_commit(&bars->kv_empty[ks]);
+        }
+        j = jn;
+      }
+      // Drain: every MMA issued above has completed before tensor memory is released.
+      mma_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, &bars->never, nullptr, kWaitNs);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = (warp - 4) >> 2;
+    const int r = ((warp & 3) << 5) + lane;
+    const int row = u.q0 + t * kBlk + r;
+    const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) << 5) << 16);
+    const uint32_t s_col = t * 128;
+    const uint32_t o_col = 256 + t * 128;
+    const float c = p.scale * kLog2e;
+    float m_run = -INFINITY, l = 0.f;
+    int n = 0;
+    bool ok = true;
+    for (int j = 0; j < jend && ok; ++j) {
+      if (!need(p, u, t, j)) continue;
+      ok = mbar_wait(&bars->s_full[t], n & 1, abort_flag, p.err, kWaitNs);
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int cchunk = 0; cchunk < 4; ++cchunk) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + s_col + cchunk * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[cchunk * 32 + i] = __uint_as_float(v[i]);
+      }
+      const int k0 = j * kBlk;
+      const bool edge = (p.causal && k0 + kBlk - 1 > u.q0 + t * kBlk) || (k0 + kBlk > u.L);
+      if (edge) {
+        const int lim_causal = p.causal ? row - k0 : kBlk - 1;     // last visible column
+        const int lim_len = u.L - 1 - k0;
+        const int lim = min(lim_causal, lim_len);
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > lim) s[i] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int i = 4; i < 128; i += 4) {
+        mx0 = fmaxf(mx0, s[i]);
+        mx1 = fmaxf(mx1, s[i + 1]);
+        mx2 = fmaxf(mx2, s[i + 2]);
+        mx3 = fmaxf(mx3, s[i + 3]);
+      }
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      float m_new = m_run;
+      if (mt > m_run + kRescaleThreshold) m_new = mt;
+      const bool changed = m_new != m_run;
+      const float alpha = changed ? ex2(m_run - m_new) : 1.f;  // m_run = -inf gives 0
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float a = ex2(fmaf(s[64 * half + 2 * i], c, -m_use));
+          const float b = ex2(fmaf(s[64 * half + 2 * i + 1], c, -m_use));
+          sum0 += a;
+          sum1 += b;
+          pk[i] = pack_bf16x2(a, b);
+        }
+        // P overwrites the first 64 columns of this tile's S region (already read).
+        tmem_st32(lane_base + s_col + 32 * half, pk);
+      }
+      l = l * alpha + (sum0 + sum1);
+      m_run = m_new;
+      // Rescale the running O (previous P V products have completed: the S MMA this
+      // warpgroup just waited for was issued after them).
+      if (n > 0 && __any_sync(0xffffffffu, changed)) {
+#pragma unroll
+        for (int cchunk = 0; cchunk < D / 32; ++cchunk) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + o_col + cchunk * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st32(lane_base + o_col + cchunk * 32, v);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[t]);
+      ++n;
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && n > 0) {
+      ok = mbar_wait(&bars->o_done[t], 0, abort_flag, p.err, kWaitNs);
+      tc_fence_after();
+    }
+    if (ok) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = row < p.N;
+      __nv_bfloat16* orow = o + (static_cast<size_t>(u.bh) * p.N + row) * D;
+#pragma unroll
+      for (int cchunk = 0; cchunk < D / 32; ++cchunk) {
+        uint32_t v[32];
+        if (n > 0) {
+          tmem_ld32(lane_base + o_col + cchunk * 32, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (store) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]) * inv, __uint_as_float(v[8 * g + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]) * inv, __uint_as_float(v[8 * g + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]) * inv, __uint_as_float(v[8 * g + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]) * inv, __uint_as_float(v[8 * g + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + cchunk * 32 + 8 * g) = w;
+          }
+        }
+      }
+      if (store)
+        lse[static_cast<size_t>(u.bh) * p.N + row] =
+            l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (bars->abort && tid == 0) {
+    // Let any bulk copy still in flight land before the CTA's shared memory is released.
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 1000000ull) {
+    }
+  }
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// [B*H, N, d] bf16 viewed as a 3-D tensor (d innermost); 64 x 128 boxes, 128B swizzle,
+// rows beyond N read as zero.
+bool make_head_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+static cudaError_t fwd_launch(const Problem& p, const void* q, const void* k, const void* v,
+                              void* o, float* lse, cudaStream_t s) {
+  CUtensorMap mq, mk, mv;
+  const int BH = p.B * p.H;
+  if (!make_head_map(&mq, q, BH, p.N, D) || !make_head_map(&mk, k, BH, p.N, D) ||
+      !make_head_map(&mv, v, BH, p.N, D))
+    return cudaErrorInvalidValue;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int nqb = (p.N + 255) / 256;
+  dim3 grid(static_cast<unsigned>(BH) * nqb);
+  fwd_sm103_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, s>>>(mq, mk, mv,
+                                                            static_cast<__nv_bfloat16*>(o), lse, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_sm103(const Problem& p, const void* q, const void* k, const void* v,
+                             void* o, float* lse, cudaStream_t s) {
+  return p.d == 64 ? fwd_launch<64>(p, q, k, v, o, lse, s)
+                   : fwd_launch<128>(p, q, k, v, o, lse, s);
+}
+
+}  // namespace fa

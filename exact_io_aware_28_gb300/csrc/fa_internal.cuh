@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libfa_gb300.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -39,6 +40,10 @@ cudaError_t launch_fwd_sm103(const Problem& p, const void* q, const void* k, con
 cudaError_t launch_bwd_sm103(const Problem& p, const void* q, const void* k, const void* v,
                              const float* lse, const void* dO, const float* D, float* dq_acc,
                              void* dk, void* dv, cudaStream_t s);
+
+// Tensor map of a [B*H, N, d] bf16 tensor (d innermost) with 64 x 128 boxes and 128-byte
+// swizzle; rows beyond N read as zero.  Returns false if the driver rejects it.
+bool make_head_map(CUtensorMap* map, const void* ptr, int BH, int N, int d);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -73,7 +73,7 @@ typedef enum {
  *                  128I..128I+127 (the block is skipped).
  *   kv_len       : NULL, or device int32 [B]; keys j >= kv_len[b] are hidden from every query of
  *                  sequence b.  Values are clamped to [0, N] on the device.
- *   scale        : multiplier of Q K^T, normally 1/sqrt(d); must be finite.
+ *   scale        : multiplier of Q K^T, normally 1/sqrt(d); must be finite and > 0.
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int H, int N, int d, int causal,

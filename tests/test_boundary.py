@@ -85,6 +85,8 @@ def bwd(**kw):
     ({"dtype": 7}, fa.FA_ERR_INVALID_ARG),
     ({"scale": float("nan")}, fa.FA_ERR_INVALID_ARG),
     ({"scale": float("inf")}, fa.FA_ERR_INVALID_ARG),
+    ({"scale": 0.0}, fa.FA_ERR_INVALID_ARG),
+    ({"scale": -0.125}, fa.FA_ERR_INVALID_ARG),
     ({"B": 300, "H": 300}, fa.FA_ERR_UNSUPPORTED),
 ])
 def test_fwd_rejects_bad_arguments(kw, code):
