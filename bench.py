@@ -14,6 +14,7 @@ timed region is bracketed by barriers and the slowest rank's time is reported.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -202,6 +203,8 @@ def run_ours(args, world, rank, local):
 
     dev = torch.device("cuda", torch.cuda.current_device())
     w = W.WORKLOADS[args.workload]
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads)
     x_cpu = W.make_inputs(w, seed=0)
     x = W.make_inputs(w, seed=0)
     x.q, x.k, x.v, x.do = (t.to(dev) for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.do))
@@ -360,6 +363,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=W.ORDER, default="long_causal")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override the workload's head count (smaller cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

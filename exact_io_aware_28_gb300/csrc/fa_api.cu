@@ -3,6 +3,7 @@
 // point allocates device memory or synchronises the stream (fa_device_error excepted).
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "fa_internal.cuh"
 
@@ -53,6 +54,19 @@ fa_status check_shape(int B, int H, int N, int d) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+unsigned long long wait_limit_ns() {
+  static unsigned long long ns = 0;
+  if (ns == 0) {
+    unsigned long long v = 2000ull;
+    if (const char* s = getenv("FA_WAIT_LIMIT_MS")) {
+      const long long ms = atoll(s);
+      if (ms > 0 && ms < 600000) v = static_cast<unsigned long long>(ms);
+    }
+    ns = v * 1000000ull;
+  }
+  return ns;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -90,7 +104,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if (!(isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
   int* err = error_word();
   if (!err) return FA_ERR_CUDA;
-  Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err};
+  Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err, wait_limit_ns()};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == FA_BF16 ? launch_fwd_sm103(p, q, k, v, o, lse, s)
                                    : launch_fwd_simt(p, dtype, q, k, v, o, lse, s);
@@ -142,7 +156,7 @@ fa_status fa_bwd_preprocess(const void* o, const void* dO, int B, int H, int N, 
   fa_status st = check_common(B, H, N, d, dtype, workspace, workspace_bytes);
   if (st != FA_OK) return st;
   if (bad_ptr(o) || bad_ptr(dO)) return FA_ERR_INVALID_ARG;
-  Problem p{B, H, N, d, 0, nullptr, nullptr, 1.f, nullptr};
+  Problem p{B, H, N, d, 0, nullptr, nullptr, 1.f, nullptr, 0};
   Workspace w = carve(workspace, B, H, N);
   return to_status(launch_bwd_preprocess(p, dtype, o, dO, w.Dsum,
                                          dtype == FA_BF16 ? w.dq_acc : nullptr,
@@ -164,9 +178,11 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* 
   if (st != FA_OK) return st;
   int* err = fa::error_word();
   if (!err) return FA_ERR_CUDA;
-  Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err};
+  Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err, wait_limit_ns()};
   Workspace w = carve(workspace, B, H, N);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == FA_BF16)
+    return to_status(launch_bwd_sm103(p, q, k, v, lse, dO, w.Dsum, w.dq_acc, dk, dv, s));
   return to_status(launch_bwd_simt(p, dtype, q, k, v, lse, dO, w.Dsum, dq, dk, dv, s));
 }
 
@@ -177,8 +193,9 @@ fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, f
   if (bad_ptr(dq)) return FA_ERR_INVALID_ARG;
   if (!(isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (dtype == FA_FP32) return FA_OK;
-  (void)stream;
-  return FA_OK;
+  Problem p{B, H, N, d, 0, nullptr, nullptr, scale, nullptr, 0};
+  Workspace w = carve(workspace, B, H, N);
+  return to_status(launch_dq_convert(p, w.dq_acc, dq, static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -39,7 +39,6 @@ using namespace ptx;
 
 constexpr int kBlk = 128;               // rows of a Q tile / keys of a K,V tile
 constexpr int kSub = 128 * 128;         // bytes of a [128 rows][64 bf16] 128B-swizzled subtile
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past a 256x growth
@@ -170,7 +169,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       bool ok = true;
       for (int j = next_any(p, u, -1, jend); ok && j >= 0; j = next_any(p, u, j, jend)) {
         for (int which = 0; which < 2 && ok; ++which) {
-          ok = mbar_wait(&bars->kv_empty[stage], (round & 1) ^ 1, abort_flag, p.err, kWaitNs);
+          ok = mbar_wait(&bars->kv_empty[stage], (round & 1) ^ 1, abort_flag, p.err, p.wait_ns);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars->kv_full[stage], C::TILE);
           const CUtensorMap* m = which == 0 ? &mk : &mv;
@@ -196,7 +195,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           if (need(p, u, t, j)) last[t] = j;
       int cs = 0, cr = 0;           // ring position consumed
       int npv[2] = {0, 0};
-      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, kWaitNs);
+      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
       auto issue_s = [&](int t, uint32_t kaddr) {
         const uint32_t qaddr = sQa + t * C::TILE;
@@ -216,7 +215,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         ++npv[t];
       };
       auto wait_full = [&]() -> bool {
-        const bool r = mbar_wait(&bars->kv_full[cs], cr & 1, abort_flag, p.err, kWaitNs);
+        const bool r = mbar_wait(&bars->kv_full[cs], cr & 1, abort_flag, p.err, p.wait_ns);
         tc_fence_after();
         return r;
       };
@@ -247,7 +246,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         int ks = -1;
         for (int t = 0; t < 2 && ok; ++t) {
           if (need(p, u, t, j)) {
-            ok = mbar_wait(&bars->p_full[t], (npv[t] & 1), abort_flag, p.err, kWaitNs);
+            ok = mbar_wait(&bars->p_full[t], (npv[t] & 1), abort_flag, p.err, p.wait_ns);
             tc_fence_after();
             if (!ok) break;
             issue_pv(t, vaddr);
@@ -274,7 +273,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       }
       // Drain: every MMA issued above has completed before tensor memory is released.
       mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, &bars->never, nullptr, kWaitNs);
+      mbar_wait(&bars->drain, 0, &bars->never, nullptr, p.wait_ns);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax warpgroups
@@ -290,7 +289,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     bool ok = true;
     for (int j = 0; j < jend && ok; ++j) {
       if (!need(p, u, t, j)) continue;
-      ok = mbar_wait(&bars->s_full[t], n & 1, abort_flag, p.err, kWaitNs);
+      ok = mbar_wait_warp(&bars->s_full[t], n & 1, abort_flag, p.err, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
       float s[128];
@@ -363,7 +362,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     }
     // ------------------------------------------------------------ epilogue
     if (ok && n > 0) {
-      ok = mbar_wait(&bars->o_done[t], 0, abort_flag, p.err, kWaitNs);
+      ok = mbar_wait_warp(&bars->o_done[t], 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
     }
     if (ok) {

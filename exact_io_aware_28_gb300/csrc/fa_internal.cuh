@@ -21,7 +21,11 @@ struct Problem {
   const int32_t* kv_len;     // [B] or nullptr
   float scale;
   int* err;                  // device error word
+  unsigned long long wait_ns;  // bound of every mbarrier wait in the tensor-core kernels
 };
+
+// Bound of device-side waits: FA_WAIT_LIMIT_MS from the environment (read once), else 2 s.
+unsigned long long wait_limit_ns();
 
 // Device error codes written into the error word (match fa_status).
 constexpr int kErrTimeout = FA_ERR_TIMEOUT;

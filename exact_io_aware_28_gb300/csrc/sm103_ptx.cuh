@@ -74,6 +74,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Warp-uniform bounded wait: every lane waits, and the warp proceeds only if all lanes
+// saw the phase complete.  Use it before warp-collective tcgen05.ld / tcgen05.st, which
+// must be executed by all 32 lanes together.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, int* err, uint64_t limit_ns) {
+  const bool ok = mbar_wait(bar, parity, abort, err, limit_ns);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
