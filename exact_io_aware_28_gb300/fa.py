@@ -20,7 +20,10 @@ FA_BF16, FA_FP32 = 0, 1
 
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_preprocess", "fa_bwd_main",
-           "fa_bwd_dq_convert", "fa_status_string", "fa_device_error")
+           "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_status_string", "fa_device_error")
+
+# Largest workspace (bytes) fa_bwd_noalloc can serve from its built-in scratch array.
+FA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class FaError(RuntimeError):
@@ -52,6 +55,8 @@ def load() -> ctypes.CDLL:
     lib.fa_bwd_main.restype = I
     lib.fa_bwd_dq_convert.argtypes = [P, I, I, I, I, F, I, P, S, P]
     lib.fa_bwd_dq_convert.restype = I
+    lib.fa_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, F, I, P]
+    lib.fa_bwd_noalloc.restype = I
     lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
     lib.fa_bwd_workspace_bytes.restype = S
     lib.fa_status_string.argtypes = [I]
@@ -156,6 +161,29 @@ def fa_bwd_dq_convert(dq, workspace, scale=None, stream=None) -> None:
                                   workspace.numel() * workspace.element_size(), _stream(stream))
     if st != FA_OK:
         raise FaError(st, "fa_bwd_dq_convert")
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, causal: bool = False, blockmask=None,
+                   kv_len=None, scale: Optional[float] = None, stream=None) -> None:
+    """fa_bwd with the library's built-in scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory.  Problems whose workspace would exceed
+    FA_NOALLOC_SCRATCH_BYTES are rejected; calls that overlap on the GPU share the array
+    and race, so serialise them.
+    """
+    _check_dense(q, k, v, o, lse, do, dq, dk, dv, blockmask, kv_len)
+    B, H, N, d = q.shape
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    st = load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, int(causal),
+                               _ptr(blockmask), _ptr(kv_len), scale, _dtype_code(q),
+                               _stream(stream))
+    if st != FA_OK:
+        need = fa_bwd_workspace_bytes(B, H, N, d)
+        if st == FA_ERR_UNSUPPORTED and need > FA_NOALLOC_SCRATCH_BYTES:
+            raise FaError(st, f"fa_bwd_noalloc: needs {need} bytes of scratch, the built-in "
+                              f"array holds {FA_NOALLOC_SCRATCH_BYTES}")
+        raise FaError(st, "fa_bwd_noalloc")
 
 
 # ----------------------------------------------------------- allocating helpers

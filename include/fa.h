@@ -127,6 +127,35 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* 
 fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, fa_dtype dtype,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Size of the library's built-in backward scratch array (64 MiB): the largest
+ * fa_bwd_workspace_bytes(B, H, N, d) that fa_bwd_noalloc accepts.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * fa_bwd without a caller-supplied workspace.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory -- code running inside
+ * another framework's memory pool without access to its allocator, plug-ins and embedded
+ * runtimes whose device memory is planned up front, or hooks where a cudaMalloc would
+ * synchronise the device or is not allowed.  It allocates nothing: the workspace is a
+ * fixed FA_NOALLOC_SCRATCH_BYTES array in the library's own device memory, which every
+ * GPU that loads the library holds until the process exits.
+ *   Arguments, layouts and results are those of fa_bwd minus the workspace.
+ *   Returns FA_ERR_UNSUPPORTED, launching nothing, when fa_bwd_workspace_bytes(B, H, N, d)
+ *   exceeds FA_NOALLOC_SCRATCH_BYTES; other errors as fa_bwd.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *   with that device current); make that first call before any stream capture.
+ *   All calls share the array and it keeps the last call's contents; every call rewrites
+ *   D and zeroes the dQ accumulator before using them.  Calls whose work overlaps on the
+ *   GPU (for example on two streams) race on the array: serialise them.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, int causal,
+                         const uint8_t* blockmask, const int32_t* kv_len,
+                         float scale, fa_dtype dtype, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 
