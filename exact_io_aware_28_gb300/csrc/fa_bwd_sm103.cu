@@ -16,14 +16,19 @@
 // the causal mask, mask[i][j] = 1 under a block mask), accumulating dK_j, dV_j in tensor
 // memory and adding each dQ_i partial to an fp32 accumulator in global memory.
 // Per query block the tensor pipe runs five MMAs (all M = 128, bf16 in, fp32 out):
-//   S^T  = K_j Q_i^T   (A: K_j K-major smem,   B: Q_i K-major smem)     -> TMEM [0,128)
-//   dP^T = V_j dO_i^T  (A: V_j K-major smem,   B: dO_i K-major smem)    -> TMEM [128,256)
-//   dV  += P^T dO_i    (A: P^T bf16 in TMEM,   B: dO_i MN-major smem)   -> TMEM [256,256+d)
-//   dK  += dS^T Q_i    (A: dS^T K-major smem,  B: Q_i MN-major smem)    -> TMEM [384,384+d)
-//   dQ_i = dS K_j      (A: dS^T MN-major smem, B: K_j MN-major smem)    -> TMEM [128,128+d)
+//   S^T  = K_j Q_i^T   (A: K_j K-major smem,    B: Q_i K-major smem)    -> TMEM [0,128)
+//   dP^T = V_j dO_i^T  (A: V_j K-major smem,    B: dO_i K-major smem)   -> TMEM [128,256)
+//   dV  += P^T dO_i    (A: P^T bf16 in TMEM,    B: dO_i MN-major smem)  -> TMEM [256,256+d)
+//   dK  += dS^T Q_i    (A: dS^T bf16 in TMEM,   B: Q_i MN-major smem)   -> TMEM [384,384+d)
+//   dQ_i = dS K_j      (A: dS^T MN-major smem,  B: K_j MN-major smem)   -> TMEM [128,128+d)
+// P^T is written over already-read S^T columns, dS^T over already-read dP^T columns.
 // Warps: 0 TMA producer (K_j, V_j once; Q_i, dO_i through a two-stage ring), 1 MMA issuer,
-// 2 tensor-memory allocation, 4-7 one thread per key row forming P^T and dS^T, 8-11 one
-// thread per query row adding dQ_i to the accumulator with vector atomics.
+// 2 tensor-memory allocation, 4-7 and 8-11 two warpgroups that each take 64 of the 128
+// query columns of every key row (phase A: P^T from S^T; phase B: dS^T from dP^T), 12-15
+// one thread per query row adding dQ_i to the accumulator with vector atomics.
+// MMA issue order per block n: dV(n), S^T(n+1), dP^T(n), dK(n), dQ(n).  The next block's
+// phase A overlaps dK(n), dQ(n); the dQ drain overlaps dV(n+1), S^T(n+2); dP^T(n) goes
+// into the columns dQ(n-1) used once that partial has been drained.
 // Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and exits.
 #include <cuda.h>
 #include <math.h>
@@ -39,7 +44,7 @@ using namespace ptx;
 constexpr int kBlk = 128;
 constexpr int kSub = 128 * 128;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 
 template <int D>
 struct Cfg {
@@ -55,12 +60,13 @@ struct Bars {
   uint64_t qdo_full[2];
   uint64_t qdo_empty[2];
   uint64_t s_full;
-  uint64_t ps_ready;
+  uint64_t dp_full;
+  uint64_t p_ready;
+  uint64_t ds_ready;
   uint64_t dq_full;
   uint64_t dq_free;
-  uint64_t ds_free;
-  uint64_t acc_done;
   uint64_t stats_full;
+  uint64_t acc_done;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -136,12 +142,13 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       mbar_init(&bars->qdo_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->ps_ready, kBlk);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, 2 * kBlk);
+    mbar_init(&bars->ds_ready, 2 * kBlk);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, kBlk);
-    mbar_init(&bars->ds_free, 1);
+    mbar_init(&bars->stats_full, 2 * kBlk);
     mbar_init(&bars->acc_done, 1);
-    mbar_init(&bars->stats_full, kBlk);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     bars->never = 0;
@@ -191,65 +198,89 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       constexpr uint32_t idKN = idesc_bf16(128, D, false, true);     // dV, dK (B MN-major)
       constexpr uint32_t idMN = idesc_bf16(128, D, true, true);      // dQ (A, B MN-major)
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aDS = smem_u32(sDS);
-      bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.err, p.wait_ns);
-      tc_fence_after();
-      int stage = 0, round = 0, n = 0;
-      for (int i = first; ok && i >= 0; i = next_q(p, u, i)) {
-        ok = mbar_wait(&bars->qdo_full[stage], round & 1, abort_flag, p.err, p.wait_ns);
-        tc_fence_after();
-        if (!ok) break;
-        const uint32_t aQ = smem_u32(sQ + stage * 2 * C::TILE);
-        const uint32_t aDO = aQ + C::TILE;
-        // S^T = K_j Q_i^T
+      const uint32_t aQ0 = smem_u32(sQ);
+      auto q_addr = [&](int n) { return aQ0 + (n & 1) * 2 * C::TILE; };
+      // TMEM column of the bf16 A operand (P^T at 0, dS^T at 128) for k-step kk: query
+      // columns 0-63 sit in the first 32 columns of the region, 64-127 in columns 64-95.
+      auto a_col = [](uint32_t region, int kk) {
+        return region + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4));
+      };
+      auto issue_s = [&](int n) {
+        const uint32_t aQ = q_addr(n);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
           mma_ss(tb, sw128_desc(aK + off, 16, 1024), sw128_desc(aQ + off, 16, 1024), idSS, kk > 0);
         }
-        // dP^T = V_j dO_i^T into the columns the previous dQ partial occupied.
-        if (n > 0) {
-          ok = mbar_wait(&bars->dq_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
-          tc_fence_after();
-          if (!ok) break;
-        }
+        mma_commit(&bars->s_full);
+      };
+      auto issue_dp = [&](int n) {
+        const uint32_t aDO = q_addr(n) + C::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
           mma_ss(tb + 128, sw128_desc(aV + off, 16, 1024), sw128_desc(aDO + off, 16, 1024), idSS,
                  kk > 0);
         }
-        mma_commit(&bars->s_full);
-        ok = mbar_wait(&bars->ps_ready, n & 1, abort_flag, p.err, p.wait_ns);
+        mma_commit(&bars->dp_full);
+      };
+      bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.err, p.wait_ns);
+      ok = ok && mbar_wait(&bars->qdo_full[0], 0, abort_flag, p.err, p.wait_ns);
+      tc_fence_after();
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
+      int n = 0;
+      for (int i = first; ok && i >= 0; ++n) {
+        const int in = next_q(p, u, i);
+        const uint32_t aQ = q_addr(n), aDO = aQ + C::TILE;
+        // dV += P^T dO_i
+        ok = mbar_wait(&bars->p_ready, n & 1, abort_flag, p.err, p.wait_ns);
         tc_fence_after();
         if (!ok) break;
-        // dV += P^T dO_i ; dK += dS^T Q_i ; dQ_i = dS K_j
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tb + 256, tb + 8 * kk, sw128_desc(aDO + 2048 * kk, kSub, 1024), idKN,
+          mma_ts(tb + 256, tb + a_col(0, kk), sw128_desc(aDO + 2048 * kk, kSub, 1024), idKN,
                  (n > 0 || kk > 0) ? 1u : 0u);
+        // S^T of the next block (its Q tile sits in the other stage of the ring).
+        if (in >= 0) {
+          ok = mbar_wait(&bars->qdo_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
+                         p.wait_ns);
+          tc_fence_after();
+          if (!ok) break;
+          issue_s(n + 1);
+        }
+        // dP^T of this block, into the columns of the drained dQ(n - 1).
+        if (n > 0) {
+          ok = mbar_wait(&bars->dq_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
+          tc_fence_after();
+          if (!ok) break;
+          issue_dp(n);
+        }
+        // dK += dS^T Q_i ; dQ_i = dS K_j
+        ok = mbar_wait(&bars->ds_ready, n & 1, abort_flag, p.err, p.wait_ns);
+        tc_fence_after();
+        if (!ok) break;
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tb + 384, sw128_desc(aDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
-                 sw128_desc(aQ + 2048 * kk, kSub, 1024), idKN, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tb + 384, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024), idKN,
+                 (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
           mma_ss(tb + 128, sw128_desc(aDS + 2048 * kk, kSub, 1024),
                  sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
         mma_commit(&bars->dq_full);
-        mma_commit(&bars->ds_free);
-        mma_commit(&bars->qdo_empty[stage]);
-        if (++stage == C::NSTAGE) {
-          stage = 0;
-          ++round;
-        }
-        ++n;
+        mma_commit(&bars->qdo_empty[n & 1]);
+        i = in;
       }
       mma_commit(&bars->acc_done);
       mma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, &bars->never, nullptr, p.wait_ns);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P^T and dS^T (key rows)
+    const int w = (warp - 4) >> 2;              // query columns [64w, 64w + 64)
     const int r = ((warp & 3) << 5) + lane;     // key row within the block = TMEM lane
     const int key = u.j * kBlk + r;
     const bool key_live = key < u.L;
@@ -258,69 +289,97 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const size_t row_off = static_cast<size_t>(u.bh) * p.N;
     bool ok = true;
     int n = 0;
-    for (int i = first; ok && i >= 0; i = next_q(p, u, i)) {
-      // The previous dS^T has been read by its dK and dQ MMAs; that also means every
-      // thread of this warpgroup has finished with the previous block's statistics.
+    for (int i = first; ok && i >= 0; i = next_q(p, u, i), ++n) {
+      // Every thread of both warpgroups has finished phase B of the previous block (and so
+      // with the statistics buffer) once ds_ready of that block has completed.
       if (n > 0) {
-        ok = mbar_wait_warp(&bars->ds_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
+        ok = mbar_wait_warp(&bars->ds_ready, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
         if (!ok) break;
       }
       // Column statistics of this query block: lse * log2(e) (+inf where the row is
       // outside the sequence or sees no key, so that P = 0 there) and D.
-      {
-        const int qrow = i * kBlk + r;
+      if (r < 64) {
+        const int col = 64 * w + r;
+        const int qrow = i * kBlk + col;
         float l2 = INFINITY, dd = 0.f;
         if (qrow < p.N) {
           const float lv = lse[row_off + qrow];
           l2 = lv == -INFINITY ? INFINITY : lv * kLog2e;
           dd = Dsum[row_off + qrow];
         }
-        sL[r] = l2;
-        sD[r] = dd;
-        mbar_arrive(&bars->stats_full);
-        ok = mbar_wait_warp(&bars->stats_full, n & 1, abort_flag, p.err, p.wait_ns);
-        if (!ok) break;
+        sL[col] = l2;
+        sD[col] = dd;
       }
+      mbar_arrive(&bars->stats_full);
+      ok = mbar_wait_warp(&bars->stats_full, n & 1, abort_flag, p.err, p.wait_ns);
+      if (!ok) break;
+      const bool diag = p.causal && i == u.j;
+      const int lim = diag ? r : 0;   // diagonal block: query column q sees key r iff q >= r
+      // ---- phase A: P^T = exp2(S^T * c - lse * log2 e) for this warpgroup's 64 columns
       ok = mbar_wait_warp(&bars->s_full, n & 1, abort_flag, p.err, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
-      const bool diag = p.causal && i == u.j;
-      const int lim = diag ? r : 0;   // diagonal block: query column q sees key r iff q >= r
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(lane_base + cc * 32, sv);
-        tmem_ld32(lane_base + 128 + cc * 32, dpv);
-        tmem_wait_ld();
-        uint32_t pp[16], dsp[16];
+      uint32_t pp[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int q0 = cc * 32 + e;
-          float pa = ex2(fmaf(__uint_as_float(sv[e]), c, -sL[q0]));
-          float pb = ex2(fmaf(__uint_as_float(sv[e + 1]), c, -sL[q0 + 1]));
-          if (!key_live || q0 < lim) pa = 0.f;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sv[32];
+        tmem_ld32_wait(lane_base + 64 * w + 32 * h, sv);
+        const float4* L4 = reinterpret_cast<const float4*>(sL + 64 * w + 32 * h);
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 l = L4[e4];
+          const int q0 = 64 * w + 32 * h + 4 * e4;
+          float pa = ex2(fmaf(__uint_as_float(sv[4 * e4 + 0]), c, -l.x));
+          float pb = ex2(fmaf(__uint_as_float(sv[4 * e4 + 1]), c, -l.y));
+          float pc = ex2(fmaf(__uint_as_float(sv[4 * e4 + 2]), c, -l.z));
+          float pd = ex2(fmaf(__uint_as_float(sv[4 * e4 + 3]), c, -l.w));
+          if (!key_live || q0 + 0 < lim) pa = 0.f;
           if (!key_live || q0 + 1 < lim) pb = 0.f;
-          const float da = pa * (__uint_as_float(dpv[e]) - sD[q0]);
-          const float db = pb * (__uint_as_float(dpv[e + 1]) - sD[q0 + 1]);
-          pp[e >> 1] = pack_bf16x2(pa, pb);
-          dsp[e >> 1] = pack_bf16x2(da, db);
+          if (!key_live || q0 + 2 < lim) pc = 0.f;
+          if (!key_live || q0 + 3 < lim) pd = 0.f;
+          pp[16 * h + 2 * e4] = pack_bf16x2(pa, pb);
+          pp[16 * h + 2 * e4 + 1] = pack_bf16x2(pc, pd);
         }
-        // P^T over the already-read S^T columns [16cc, 16cc + 16).
-        tmem_st16(lane_base + cc * 16, pp);
-        // dS^T row r, columns 32cc .. 32cc + 31, into the swizzled shared tile.
+      }
+      // P^T over this warpgroup's own, already-read S^T columns [64w, 64w + 32).
+      tmem_st32(lane_base + 64 * w, pp);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+      // ---- phase B: dS^T = P^T o (dP^T - D)
+      ok = mbar_wait_warp(&bars->dp_full, n & 1, abort_flag, p.err, p.wait_ns);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t dpv[32], dsp[16];
+        tmem_ld32_wait(lane_base + 128 + 64 * w + 32 * h, dpv);
+        const float4* D4 = reinterpret_cast<const float4*>(sD + 64 * w + 32 * h);
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 dd = D4[e4];
+          const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * h + 2 * e4]));
+          const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * h + 2 * e4 + 1]));
+          dsp[2 * e4] = pack_bf16x2(p01.x * (__uint_as_float(dpv[4 * e4 + 0]) - dd.x),
+                                    p01.y * (__uint_as_float(dpv[4 * e4 + 1]) - dd.y));
+          dsp[2 * e4 + 1] = pack_bf16x2(p23.x * (__uint_as_float(dpv[4 * e4 + 2]) - dd.z),
+                                        p23.y * (__uint_as_float(dpv[4 * e4 + 3]) - dd.w));
+        }
+        // dS^T over this warpgroup's already-read dP^T columns, and into the swizzled
+        // shared tile (row r, query columns 64w + 32h ...).
+        tmem_st16(lane_base + 128 + 64 * w + 16 * h, dsp);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          uint4 w = make_uint4(dsp[4 * g], dsp[4 * g + 1], dsp[4 * g + 2], dsp[4 * g + 3]);
-          *reinterpret_cast<uint4*>(sDS + sw128_offset(r, cc * 32 + 8 * g)) = w;
+          uint4 v4 = make_uint4(dsp[4 * g], dsp[4 * g + 1], dsp[4 * g + 2], dsp[4 * g + 3]);
+          *reinterpret_cast<uint4*>(sDS + sw128_offset(r, 64 * w + 32 * h + 8 * g)) = v4;
         }
       }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->ps_ready);
-      ++n;
+      mbar_arrive(&bars->ds_ready);
     }
-    // ------------------------------------------------------------ dK, dV epilogue
+    // ------------------------------------------------------------ dK (w = 0), dV (w = 1)
     if (ok && n > 0) {
       ok = mbar_wait_warp(&bars->acc_done, 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
@@ -328,37 +387,31 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     // TMEM loads are warp-collective: every lane loads, only rows inside the sequence store.
     if (ok) {
       const bool store = key < p.N;
-      __nv_bfloat16* dkrow = dk + (row_off + key) * D;
-      __nv_bfloat16* dvrow = dv + (row_off + key) * D;
+      const float mul = w == 0 ? p.scale : 1.f;
+      __nv_bfloat16* dst = (w == 0 ? dk : dv) + (row_off + key) * D;
+      const uint32_t col0 = w == 0 ? 384u : 256u;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t a[32], b[32];
+        uint32_t a[32];
         if (n > 0) {
-          tmem_ld32(lane_base + 384 + cc * 32, a);
-          tmem_ld32(lane_base + 256 + cc * 32, b);
-          tmem_wait_ld();
+          tmem_ld32_wait(lane_base + col0 + cc * 32, a);
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a[e] = b[e] = 0u;
+          for (int e = 0; e < 32; ++e) a[e] = 0u;
         }
         if (!store) continue;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          uint4 wk, wv;
-          wk.x = pack_bf16x2(__uint_as_float(a[8 * g]) * p.scale, __uint_as_float(a[8 * g + 1]) * p.scale);
-          wk.y = pack_bf16x2(__uint_as_float(a[8 * g + 2]) * p.scale, __uint_as_float(a[8 * g + 3]) * p.scale);
-          wk.z = pack_bf16x2(__uint_as_float(a[8 * g + 4]) * p.scale, __uint_as_float(a[8 * g + 5]) * p.scale);
-          wk.w = pack_bf16x2(__uint_as_float(a[8 * g + 6]) * p.scale, __uint_as_float(a[8 * g + 7]) * p.scale);
-          wv.x = pack_bf16x2(__uint_as_float(b[8 * g]), __uint_as_float(b[8 * g + 1]));
-          wv.y = pack_bf16x2(__uint_as_float(b[8 * g + 2]), __uint_as_float(b[8 * g + 3]));
-          wv.z = pack_bf16x2(__uint_as_float(b[8 * g + 4]), __uint_as_float(b[8 * g + 5]));
-          wv.w = pack_bf16x2(__uint_as_float(b[8 * g + 6]), __uint_as_float(b[8 * g + 7]));
-          *reinterpret_cast<uint4*>(dkrow + cc * 32 + 8 * g) = wk;
-          *reinterpret_cast<uint4*>(dvrow + cc * 32 + 8 * g) = wv;
+          uint4 wv;
+          wv.x = pack_bf16x2(__uint_as_float(a[8 * g]) * mul, __uint_as_float(a[8 * g + 1]) * mul);
+          wv.y = pack_bf16x2(__uint_as_float(a[8 * g + 2]) * mul, __uint_as_float(a[8 * g + 3]) * mul);
+          wv.z = pack_bf16x2(__uint_as_float(a[8 * g + 4]) * mul, __uint_as_float(a[8 * g + 5]) * mul);
+          wv.w = pack_bf16x2(__uint_as_float(a[8 * g + 6]) * mul, __uint_as_float(a[8 * g + 7]) * mul);
+          *reinterpret_cast<uint4*>(dst + cc * 32 + 8 * g) = wv;
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ partials (query rows)
     const int r = ((warp & 3) << 5) + lane;
     const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) << 5) << 16);
@@ -369,16 +422,15 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       if (!ok) break;
       tc_fence_after();
       const int qrow = i * kBlk + r;
-      float* dst = dq_acc + (static_cast<size_t>(u.bh) * p.N + qrow) * D;
+      float* dstq = dq_acc + (static_cast<size_t>(u.bh) * p.N + qrow) * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t v[32];
-        tmem_ld32(lane_base + 128 + cc * 32, v);
-        tmem_wait_ld();
+        tmem_ld32_wait(lane_base + 128 + cc * 32, v);
         if (qrow < p.N) {
 #pragma unroll
           for (int g = 0; g < 8; ++g)
-            atomicAdd(reinterpret_cast<float4*>(dst + cc * 32 + 4 * g),
+            atomicAdd(reinterpret_cast<float4*>(dstq + cc * 32 + 4 * g),
                       make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
                                   __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
         }

@@ -293,13 +293,11 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       if (!ok) break;
       tc_fence_after();
       float s[128];
+      {
+        uint32_t v[128];
+        tmem_ld128_wait(lane_base + s_col, v);
 #pragma unroll
-      for (int cchunk = 0; cchunk < 4; ++cchunk) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + s_col + cchunk * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[cchunk * 32 + i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(v[i]);
       }
       const int k0 = j * kBlk;
       const bool edge = (p.causal && k0 + kBlk - 1 > u.q0 + t * kBlk) || (k0 + kBlk > u.L);
@@ -348,8 +346,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 #pragma unroll
         for (int cchunk = 0; cchunk < D / 32; ++cchunk) {
           uint32_t v[32];
-          tmem_ld32(lane_base + o_col + cchunk * 32, v);
-          tmem_wait_ld();
+          tmem_ld32_wait(lane_base + o_col + cchunk * 32, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
           tmem_st32(lane_base + o_col + cchunk * 32, v);
@@ -373,8 +370,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       for (int cchunk = 0; cchunk < D / 32; ++cchunk) {
         uint32_t v[32];
         if (n > 0) {
-          tmem_ld32(lane_base + o_col + cchunk * 32, v);
-          tmem_wait_ld();
+          tmem_ld32_wait(lane_base + o_col + cchunk * 32, v);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
