@@ -20,12 +20,16 @@
 //   dP^T = V_j dO_i^T  (A: V_j K-major smem,    B: dO_i K-major smem)   -> TMEM [128,256)
 //   dV  += P^T dO_i    (A: P^T bf16 in TMEM,    B: dO_i MN-major smem)  -> TMEM [256,256+d)
 //   dK  += dS^T Q_i    (A: dS^T bf16 in TMEM,   B: Q_i MN-major smem)   -> TMEM [384,384+d)
-//   dQ_i = dS K_j      (A: dS^T MN-major smem,  B: K_j MN-major smem)   -> TMEM [128,128+d)
+//   d = 128: dQ_i^T = K_j^T dS^T (A: K_j MN-major smem, B: dS^T MN-major smem) -> TMEM [128,256)
+//   d = 64:  dQ_i   = dS K_j     (A: dS^T MN-major smem, B: K_j MN-major smem) -> TMEM [128,192)
 // P^T is written over already-read S^T columns, dS^T over already-read dP^T columns.
 // Warps: 0 TMA producer (K_j, V_j once; Q_i, dO_i through a two-stage ring), 1 MMA issuer,
 // 2 tensor-memory allocation, 4-7 and 8-11 two warpgroups that each take 64 of the 128
 // query columns of every key row (phase A: P^T from S^T; phase B: dS^T from dP^T), 12-15
-// one thread per query row adding dQ_i to the accumulator with vector atomics.
+// the dQ drain.  With d = 128 the partial is produced transposed (TMEM lane = head dimension),
+// so each warp's atomics cover 32 consecutive floats of one accumulator row (one 128-byte
+// segment) instead of touching 32 rows; with d = 64 one thread per query row adds 16-byte
+// vectors.
 // MMA issue order per block n: dV(n), S^T(n+1), dP^T(n), dK(n), dQ(n).  The next block's
 // phase A overlaps dK(n), dQ(n); the dQ drain overlaps dV(n+1), S^T(n+2); dP^T(n) goes
 // into the columns dQ(n-1) used once that partial has been drained.
@@ -197,6 +201,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idKN = idesc_bf16(128, D, false, true);     // dV, dK (B MN-major)
       constexpr uint32_t idMN = idesc_bf16(128, D, true, true);      // dQ (A, B MN-major)
+      constexpr uint32_t idQT = idesc_bf16(128, 128, true, true);    // dQ^T (A, B MN-major)
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aDS = smem_u32(sDS);
       const uint32_t aQ0 = smem_u32(sQ);
       auto q_addr = [&](int n) { return aQ0 + (n & 1) * 2 * C::TILE; };
@@ -266,10 +271,18 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         for (int kk = 0; kk < kBlk / 16; ++kk)
           mma_ts(tb + 384, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024), idKN,
                  (n > 0 || kk > 0) ? 1u : 0u);
+        if constexpr (D == 128) {
+          // dQ^T = K_j^T dS^T: M = head dimension, N = query row, K = key row.
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tb + 128, sw128_desc(aDS + 2048 * kk, kSub, 1024),
-                 sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ss(tb + 128, sw128_desc(aK + 2048 * kk, kSub, 1024),
+                   sw128_desc(aDS + 2048 * kk, kSub, 1024), idQT, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ss(tb + 128, sw128_desc(aDS + 2048 * kk, kSub, 1024),
+                   sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
+        }
         mma_commit(&bars->dq_full);
         mma_commit(&bars->qdo_empty[n & 1]);
         i = in;
@@ -421,18 +434,33 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       ok = mbar_wait_warp(&bars->dq_full, n & 1, abort_flag, p.err, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
-      const int qrow = i * kBlk + r;
-      float* dstq = dq_acc + (static_cast<size_t>(u.bh) * p.N + qrow) * D;
+      if constexpr (D == 128) {
+        // Lane = head dimension r; columns = the block's 128 query rows.
+        const int q0 = i * kBlk;
+        float* dcol = dq_acc + (static_cast<size_t>(u.bh) * p.N + q0) * D + r;
+        const int qn = min(kBlk, p.N - q0);
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld32_wait(lane_base + 128 + cc * 32, v);
-        if (qrow < p.N) {
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32_wait(lane_base + 128 + cc * 32, v);
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            atomicAdd(reinterpret_cast<float4*>(dstq + cc * 32 + 4 * g),
-                      make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
-                                  __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
+          for (int e = 0; e < 32; ++e)
+            if (cc * 32 + e < qn) atomicAdd(dcol + static_cast<size_t>(cc * 32 + e) * D, __uint_as_float(v[e]));
+        }
+      } else {
+        const int qrow = i * kBlk + r;
+        float* dstq = dq_acc + (static_cast<size_t>(u.bh) * p.N + qrow) * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32_wait(lane_base + 128 + cc * 32, v);
+          if (qrow < p.N) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              atomicAdd(reinterpret_cast<float4*>(dstq + cc * 32 + 4 * g),
+                        make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                    __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
+          }
         }
       }
       tc_fence_before();
