@@ -107,7 +107,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-                 const float* __restrict__ lse, const float* __restrict__ Dsum,
+                 const __grid_constant__ CUtensorMap mdq, const float* __restrict__ lse, const float* __restrict__ Dsum,
                  float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dk,
                  __nv_bfloat16* __restrict__ dv, Problem p) {
   using C = Cfg<D>;
@@ -435,18 +435,34 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       if (!ok) break;
       tc_fence_after();
       if constexpr (D == 128) {
-        // Lane = head dimension r; columns = the block's 128 query rows.
+        // Lane = head dimension; columns = the block's 128 query rows.  Each warp stages
+        // its 32 dimensions x 32 query rows chunk as a [32 q][32 d] fp32 box in the dS^T
+        // tile (idle from the dQ MMA's completion until the next phase B) and hands it to
+        // the TMA unit as a bulk reduce-add into the accumulator.
         const int q0 = i * kBlk;
-        float* dcol = dq_acc + (static_cast<size_t>(u.bh) * p.N + q0) * D + r;
-        const int qn = min(kBlk, p.N - q0);
+        const int wq = warp & 3;
+        float* stage0 = reinterpret_cast<float*>(sDS) + wq * 2048;   // 2 x [32][32] per warp
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t v[32];
           tmem_ld32_wait(lane_base + 128 + cc * 32, v);
+          float* st = stage0 + (cc & 1) * 1024;
+          if (cc >= 2) {  // the reduce that read this buffer two chunks ago is done with it
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+          }
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (cc * 32 + e < qn) atomicAdd(dcol + static_cast<size_t>(cc * 32 + e) * D, __uint_as_float(v[e]));
+          for (int e = 0; e < 32; ++e) st[e * 32 + lane] = __uint_as_float(v[e]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && q0 + cc * 32 < p.N) {
+            tma_reduce_add_3d(&mdq, st, 32 * wq, q0 + cc * 32, u.bh);
+            bulk_commit_group();
+          }
         }
+        // The staging buffers (the dS^T tile) are reused by the next phase B.
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
       } else {
         const int qrow = i * kBlk + r;
         float* dstq = dq_acc + (static_cast<size_t>(u.bh) * p.N + qrow) * D;
@@ -469,6 +485,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     }
   }
 
+  if (D == 128 && warp >= 12 && lane == 0) bulk_wait_group_all();
   tc_fence_before();
   __syncthreads();
   if (bars->abort && tid == 0) {
@@ -488,10 +505,11 @@ template <int D>
 cudaError_t bwd_launch(const Problem& p, const void* q, const void* k, const void* v,
                        const float* lse, const void* dO, const float* Dsum, float* dq_acc,
                        void* dk, void* dv, cudaStream_t s) {
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   const int BH = p.B * p.H;
   if (!make_head_map(&mq, q, BH, p.N, D) || !make_head_map(&mk, k, BH, p.N, D) ||
-      !make_head_map(&mv, v, BH, p.N, D) || !make_head_map(&mdo, dO, BH, p.N, D))
+      !make_head_map(&mv, v, BH, p.N, D) || !make_head_map(&mdo, dO, BH, p.N, D) ||
+      !make_acc_map(&mdq, dq_acc, BH, p.N, D))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -505,7 +523,7 @@ cudaError_t bwd_launch(const Problem& p, const void* q, const void* k, const voi
   const int nkb = (p.N + kBlk - 1) / kBlk;
   dim3 grid(static_cast<unsigned>(BH) * nkb);
   bwd_sm103_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, s>>>(
-      mq, mk, mv, mdo, lse, Dsum, dq_acc, static_cast<__nv_bfloat16*>(dk),
+      mq, mk, mv, mdo, mdq, lse, Dsum, dq_acc, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), p);
   return cudaGetLastError();
 }
