@@ -23,16 +23,17 @@
 //   d = 128: dQ_i^T = K_j^T dS^T (A: K_j MN-major smem, B: dS^T MN-major smem) -> TMEM [128,256)
 //   d = 64:  dQ_i   = dS K_j     (A: dS^T MN-major smem, B: K_j MN-major smem) -> TMEM [128,192)
 // P^T is written over already-read S^T columns, dS^T over already-read dP^T columns.
-// Warps: 0 TMA producer (K_j, V_j once; Q_i, dO_i through a two-stage ring), 1 MMA issuer,
-// 2 tensor-memory allocation, 4-7 and 8-11 two warpgroups that each take 64 of the 128
-// query columns of every key row (phase A: P^T from S^T; phase B: dS^T from dP^T), 12-15
-// the dQ drain.  With d = 128 the partial is produced transposed (TMEM lane = head dimension),
+// Warps (16): 0-3 the dQ drain, 4-7 and 8-11
+// two warpgroups that each take 64 of the 128 query columns of every key row (phase A: P^T
+// from S^T; phase B: dS^T from dP^T), 12 TMA producer (K_j, V_j once; Q_i and dO_i through
+// two-stage rings) and tensor-memory allocation, 13 MMA issuer, 14-15 idle.  With d = 128 the partial is produced transposed (TMEM lane = head dimension),
 // so each warp's atomics cover 32 consecutive floats of one accumulator row (one 128-byte
 // segment) instead of touching 32 rows; with d = 64 one thread per query row adds 16-byte
 // vectors.
-// MMA issue order per block n: dV(n), S^T(n+1), dP^T(n), dK(n), dQ(n).  The next block's
-// phase A overlaps dK(n), dQ(n); the dQ drain overlaps dV(n+1), S^T(n+2); dP^T(n) goes
-// into the columns dQ(n-1) used once that partial has been drained.
+// MMA issue order per block n: dV(n), S^T(n+1), dK(n), dQ(n), dP^T(n+1).  dP^T(n+1) goes
+// into the columns of dQ(n) as soon as the drain has copied them out, so the next block's
+// phase B can follow its phase A directly; dV(n+1) and S^T(n+2) then run during that
+// phase B, dK(n+1) and dQ(n+1) during the following phase A.
 // Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and exits.
 #include <cuda.h>
 #include <math.h>
@@ -48,6 +49,8 @@ using namespace ptx;
 constexpr int kBlk = 128;
 constexpr int kSub = 128 * 128;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kProducerWarp = 12;  // also allocates tensor memory
+constexpr int kMmaWarp = 13;       // warps 14-15 idle
 constexpr int kThreads = 512;
 
 template <int D>
@@ -61,8 +64,10 @@ struct Cfg {
 
 struct Bars {
   uint64_t kv_full;
-  uint64_t qdo_full[2];
-  uint64_t qdo_empty[2];
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t do_full[2];
+  uint64_t do_empty[2];
   uint64_t s_full;
   uint64_t dp_full;
   uint64_t p_ready;
@@ -70,6 +75,7 @@ struct Bars {
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t stats_full;
+  uint64_t sds_free;
   uint64_t acc_done;
   uint64_t drain;
   uint32_t tmem_base;
@@ -142,8 +148,12 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   if (tid == 0) {
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->qdo_full[s], 1);
-      mbar_init(&bars->qdo_empty[s], 1);
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->do_full[s], 1);
+      // Released by the MMA commit and by the two dQ-drain warps that stage their partial
+      // in the dO stage once its MMAs are done.
+      mbar_init(&bars->do_empty[s], 3);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
@@ -152,13 +162,14 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, kBlk);
     mbar_init(&bars->stats_full, 2 * kBlk);
+    mbar_init(&bars->sds_free, 2);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     bars->never = 0;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == kProducerWarp) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
@@ -168,7 +179,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   const uint32_t tb = bars->tmem_base;
   const int first = next_q(p, u, -1);
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && first >= 0) {
       tma_prefetch_desc(&mq);
@@ -180,28 +191,30 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       }
       int stage = 0, round = 0;
       for (int i = first; i >= 0; i = next_q(p, u, i)) {
-        if (!mbar_wait(&bars->qdo_empty[stage], (round & 1) ^ 1, abort_flag, p.err, p.wait_ns))
-          break;
-        mbar_arrive_expect_tx(&bars->qdo_full[stage], 2 * C::TILE);
         uint8_t* dst = sQ + stage * 2 * C::TILE;
-        for (int s = 0; s < C::NSUB; ++s) {
-          tma_load_3d(dst + s * kSub, &mq, &bars->qdo_full[stage], 64 * s, i * kBlk, u.bh);
-          tma_load_3d(dst + C::TILE + s * kSub, &mdo, &bars->qdo_full[stage], 64 * s, i * kBlk,
+        if (!mbar_wait(&bars->q_empty[stage], (round & 1) ^ 1, abort_flag, p.err, p.wait_ns))
+          break;
+        mbar_arrive_expect_tx(&bars->q_full[stage], C::TILE);
+        for (int s = 0; s < C::NSUB; ++s)
+          tma_load_3d(dst + s * kSub, &mq, &bars->q_full[stage], 64 * s, i * kBlk, u.bh);
+        if (!mbar_wait(&bars->do_empty[stage], (round & 1) ^ 1, abort_flag, p.err, p.wait_ns))
+          break;
+        mbar_arrive_expect_tx(&bars->do_full[stage], C::TILE);
+        for (int s = 0; s < C::NSUB; ++s)
+          tma_load_3d(dst + C::TILE + s * kSub, &mdo, &bars->do_full[stage], 64 * s, i * kBlk,
                       u.bh);
-        }
         if (++stage == C::NSTAGE) {
           stage = 0;
           ++round;
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && first >= 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idKN = idesc_bf16(128, D, false, true);     // dV, dK (B MN-major)
       constexpr uint32_t idMN = idesc_bf16(128, D, true, true);      // dQ (A, B MN-major)
-      constexpr uint32_t idQT = idesc_bf16(128, 128, true, true);    // dQ^T (A, B MN-major)
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aDS = smem_u32(sDS);
       const uint32_t aQ0 = smem_u32(sQ);
       auto q_addr = [&](int n) { return aQ0 + (n & 1) * 2 * C::TILE; };
@@ -230,17 +243,17 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         mma_commit(&bars->dp_full);
       };
       bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.err, p.wait_ns);
-      ok = ok && mbar_wait(&bars->qdo_full[0], 0, abort_flag, p.err, p.wait_ns);
+      ok = ok && mbar_wait(&bars->q_full[0], 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
-      if (ok) {
-        issue_s(0);
-        issue_dp(0);
-      }
+      if (ok) issue_s(0);
+      ok = ok && mbar_wait(&bars->do_full[0], 0, abort_flag, p.err, p.wait_ns);
+      tc_fence_after();
+      if (ok) issue_dp(0);
       int n = 0;
       for (int i = first; ok && i >= 0; ++n) {
         const int in = next_q(p, u, i);
         const uint32_t aQ = q_addr(n), aDO = aQ + C::TILE;
-        // dV += P^T dO_i
+        // dV += P^T dO_i  (dO_i was waited for before dP^T(n))
         ok = mbar_wait(&bars->p_ready, n & 1, abort_flag, p.err, p.wait_ns);
         tc_fence_after();
         if (!ok) break;
@@ -250,18 +263,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                  (n > 0 || kk > 0) ? 1u : 0u);
         // S^T of the next block (its Q tile sits in the other stage of the ring).
         if (in >= 0) {
-          ok = mbar_wait(&bars->qdo_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
+          ok = mbar_wait(&bars->q_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
                          p.wait_ns);
           tc_fence_after();
           if (!ok) break;
           issue_s(n + 1);
-        }
-        // dP^T of this block, into the columns of the drained dQ(n - 1).
-        if (n > 0) {
-          ok = mbar_wait(&bars->dq_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
-          tc_fence_after();
-          if (!ok) break;
-          issue_dp(n);
         }
         // dK += dS^T Q_i ; dQ_i = dS K_j
         ok = mbar_wait(&bars->ds_ready, n & 1, abort_flag, p.err, p.wait_ns);
@@ -271,20 +277,23 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         for (int kk = 0; kk < kBlk / 16; ++kk)
           mma_ts(tb + 384, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024), idKN,
                  (n > 0 || kk > 0) ? 1u : 0u);
-        if constexpr (D == 128) {
-          // dQ^T = K_j^T dS^T: M = head dimension, N = query row, K = key row.
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ss(tb + 128, sw128_desc(aK + 2048 * kk, kSub, 1024),
-                   sw128_desc(aDS + 2048 * kk, kSub, 1024), idQT, kk > 0);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ss(tb + 128, sw128_desc(aDS + 2048 * kk, kSub, 1024),
-                   sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
-        }
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ss(tb + 128, sw128_desc(aDS + 2048 * kk, kSub, 1024),
+                 sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
         mma_commit(&bars->dq_full);
-        mma_commit(&bars->qdo_empty[n & 1]);
+        mma_commit(&bars->q_empty[n & 1]);
+        mma_commit(&bars->do_empty[n & 1]);
+        // dP^T of the next block, into the columns of dQ(n) as soon as the drain has read
+        // them, so that its phase B can follow its phase A without waiting for dV and S^T.
+        if (in >= 0) {
+          ok = mbar_wait(&bars->dq_free, n & 1, abort_flag, p.err, p.wait_ns);
+          ok = ok && mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag,
+                               p.err, p.wait_ns);
+          tc_fence_after();
+          if (!ok) break;
+          issue_dp(n + 1);
+        }
         i = in;
       }
       mma_commit(&bars->acc_done);
@@ -300,6 +309,18 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) << 5) << 16);
     const float c = p.scale * kLog2e;
     const size_t row_off = static_cast<size_t>(u.bh) * p.N;
+    float st_l2 = INFINITY, st_dd = 0.f;
+    auto load_stats = [&](int iq) {
+      st_l2 = INFINITY;
+      st_dd = 0.f;
+      const int qrow = iq * kBlk + 64 * w + r;
+      if (iq >= 0 && qrow < p.N) {
+        const float lv = lse[row_off + qrow];
+        st_l2 = lv == -INFINITY ? INFINITY : lv * kLog2e;
+        st_dd = Dsum[row_off + qrow];
+      }
+    };
+    if (r < 64) load_stats(first);
     bool ok = true;
     int n = 0;
     for (int i = first; ok && i >= 0; i = next_q(p, u, i), ++n) {
@@ -310,18 +331,12 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         if (!ok) break;
       }
       // Column statistics of this query block: lse * log2(e) (+inf where the row is
-      // outside the sequence or sees no key, so that P = 0 there) and D.
+      // outside the sequence or sees no key, so that P = 0 there) and D.  They were loaded
+      // into registers during the previous block; the next block's are requested now.
       if (r < 64) {
-        const int col = 64 * w + r;
-        const int qrow = i * kBlk + col;
-        float l2 = INFINITY, dd = 0.f;
-        if (qrow < p.N) {
-          const float lv = lse[row_off + qrow];
-          l2 = lv == -INFINITY ? INFINITY : lv * kLog2e;
-          dd = Dsum[row_off + qrow];
-        }
-        sL[col] = l2;
-        sD[col] = dd;
+        sL[64 * w + r] = st_l2;
+        sD[64 * w + r] = st_dd;
+        load_stats(next_q(p, u, i));
       }
       mbar_arrive(&bars->stats_full);
       ok = mbar_wait_warp(&bars->stats_full, n & 1, abort_flag, p.err, p.wait_ns);
@@ -333,25 +348,28 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       if (!ok) break;
       tc_fence_after();
       uint32_t pp[32];
+      // Off the diagonal, every query column of a live key row is visible: no masks.
+      const bool masked = diag || !key_live;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t sv[32];
         tmem_ld32_wait(lane_base + 64 * w + 32 * h, sv);
-        const float4* L4 = reinterpret_cast<const float4*>(sL + 64 * w + 32 * h);
+        const float* L = sL + 64 * w + 32 * h;
+        if (!masked) {
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l = L4[e4];
-          const int q0 = 64 * w + 32 * h + 4 * e4;
-          float pa = ex2(fmaf(__uint_as_float(sv[4 * e4 + 0]), c, -l.x));
-          float pb = ex2(fmaf(__uint_as_float(sv[4 * e4 + 1]), c, -l.y));
-          float pc = ex2(fmaf(__uint_as_float(sv[4 * e4 + 2]), c, -l.z));
-          float pd = ex2(fmaf(__uint_as_float(sv[4 * e4 + 3]), c, -l.w));
-          if (!key_live || q0 + 0 < lim) pa = 0.f;
-          if (!key_live || q0 + 1 < lim) pb = 0.f;
-          if (!key_live || q0 + 2 < lim) pc = 0.f;
-          if (!key_live || q0 + 3 < lim) pd = 0.f;
-          pp[16 * h + 2 * e4] = pack_bf16x2(pa, pb);
-          pp[16 * h + 2 * e4 + 1] = pack_bf16x2(pc, pd);
+          for (int e = 0; e < 32; e += 2)
+            pp[16 * h + e / 2] = pack_bf16x2(ex2(fmaf(__uint_as_float(sv[e]), c, -L[e])),
+                                             ex2(fmaf(__uint_as_float(sv[e + 1]), c, -L[e + 1])));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int q0 = 64 * w + 32 * h + e;
+            float pa = ex2(fmaf(__uint_as_float(sv[e]), c, -L[e]));
+            float pb = ex2(fmaf(__uint_as_float(sv[e + 1]), c, -L[e + 1]));
+            if (!key_live || q0 < lim) pa = 0.f;
+            if (!key_live || q0 + 1 < lim) pb = 0.f;
+            pp[16 * h + e / 2] = pack_bf16x2(pa, pb);
+          }
         }
       }
       // P^T over this warpgroup's own, already-read S^T columns [64w, 64w + 32).
@@ -361,6 +379,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       mbar_arrive(&bars->p_ready);
       // ---- phase B: dS^T = P^T o (dP^T - D)
       ok = mbar_wait_warp(&bars->dp_full, n & 1, abort_flag, p.err, p.wait_ns);
+      // Two drain warps staged the previous dQ partial in the dS^T tile.
+      if (ok && n > 0) ok = mbar_wait_warp(&bars->sds_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -424,9 +444,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
       }
     }
-  } else if (warp >= 12) {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ dQ partials (query rows)
-    const int r = ((warp & 3) << 5) + lane;
     const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) << 5) << 16);
     bool ok = true;
     int n = 0;
@@ -434,58 +453,45 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       ok = mbar_wait_warp(&bars->dq_full, n & 1, abort_flag, p.err, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
-      if constexpr (D == 128) {
-        // Lane = head dimension; columns = the block's 128 query rows.  Each warp stages
-        // its 32 dimensions x 32 query rows chunk as a [32 q][32 d] fp32 box in the dS^T
-        // tile (idle from the dQ MMA's completion until the next phase B) and hands it to
-        // the TMA unit as a bulk reduce-add into the accumulator.
-        const int q0 = i * kBlk;
-        const int wq = warp & 3;
-        float* stage0 = reinterpret_cast<float*>(sDS) + wq * 2048;   // 2 x [32][32] per warp
+      // Lane = query row.  Each warp copies its 32 rows x d columns of the partial out of
+      // TMEM into [32 q][32 d] fp32 boxes with the 128-byte swizzle (16-byte stores, no bank
+      // conflicts), releases the TMEM columns at once, and hands the boxes to the TMA unit
+      // as bulk reduce-adds into the accumulator.  Warps 0-1 stage in this block's dO stage
+      // (its MMAs are done with it; the next dO load into it waits for these reads), warps
+      // 2-3 in the dS^T tile (the next phase B waits for these reads).
+      const int wq = warp & 3;
+      const int q0 = i * kBlk + 32 * wq;
+      uint8_t* st = wq < 2 ? sQ + (n & 1) * 2 * C::TILE + C::TILE + wq * (D / 32) * 4096
+                           : sDS + (wq - 2) * (D / 32) * 4096;
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[32];
-          tmem_ld32_wait(lane_base + 128 + cc * 32, v);
-          float* st = stage0 + (cc & 1) * 1024;
-          if (cc >= 2) {  // the reduce that read this buffer two chunks ago is done with it
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-          }
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32_wait(lane_base + 128 + cc * 32, v);
+        uint8_t* row = st + cc * 4096 + lane * 128;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) st[e * 32 + lane] = __uint_as_float(v[e]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && q0 + cc * 32 < p.N) {
-            tma_reduce_add_3d(&mdq, st, 32 * wq, q0 + cc * 32, u.bh);
-            bulk_commit_group();
-          }
-        }
-        // The staging buffers (the dS^T tile) are reused by the next phase B.
-        if (lane == 0) bulk_wait_group_read<0>();
-        __syncwarp();
-      } else {
-        const int qrow = i * kBlk + r;
-        float* dstq = dq_acc + (static_cast<size_t>(u.bh) * p.N + qrow) * D;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld32_wait(lane_base + 128 + cc * 32, v);
-          if (qrow < p.N) {
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-              atomicAdd(reinterpret_cast<float4*>(dstq + cc * 32 + 4 * g),
-                        make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
-                                    __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
-          }
-        }
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
+              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       }
       tc_fence_before();
       mbar_arrive(&bars->dq_free);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (q0 < p.N) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_3d(&mdq, st + cc * 4096, 32 * cc, q0, u.bh);
+          bulk_commit_group();
+          bulk_wait_group_read<0>();
+        }
+        mbar_arrive(wq < 2 ? &bars->do_empty[n & 1] : &bars->sds_free);
+      }
+      __syncwarp();
       ++n;
     }
   }
 
-  if (D == 128 && warp >= 12 && lane == 0) bulk_wait_group_all();
+  if (warp < 4 && lane == 0) bulk_wait_group_all();
   tc_fence_before();
   __syncthreads();
   if (bars->abort && tid == 0) {
@@ -495,7 +501,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     }
   }
   __syncthreads();
-  if (warp == 2) {
+  if (warp == kProducerWarp) {
     tc_fence_after();
     tmem_dealloc(tb, 512);
   }

@@ -438,8 +438,9 @@ bool make_head_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [B*H, N, d] fp32 accumulator as a 3-D tensor with 32 x 32 boxes, no swizzle; rows beyond
-// N are outside the map, so a reduce box that overhangs the sequence end is clipped.
+// [B*H, N, d] fp32 accumulator as a 3-D tensor with 32 x 32 boxes (128-byte rows, 128-byte
+// swizzle); rows beyond N are outside the map, so a box that overhangs the sequence end is
+// clipped.
 bool make_acc_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -449,7 +450,7 @@ bool make_acc_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
   cuuint32_t box[3] = {32, 32, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -49,7 +49,7 @@ cudaError_t launch_bwd_sm103(const Problem& p, const void* q, const void* k, con
 // swizzle; rows beyond N read as zero.  Returns false if the driver rejects it.
 bool make_head_map(CUtensorMap* map, const void* ptr, int BH, int N, int d);
 
-// Tensor map of a [B*H, N, d] fp32 accumulator with 32 x 32 boxes (no swizzle), for bulk
+// Tensor map of a [B*H, N, d] fp32 accumulator with 32 x 32 boxes (128-byte swizzle), for bulk
 // reduce-add; rows beyond N are outside the map.
 bool make_acc_map(CUtensorMap* map, const void* ptr, int BH, int N, int d);
 
