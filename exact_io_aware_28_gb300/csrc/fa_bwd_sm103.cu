@@ -478,7 +478,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        if (q0 < p.N) {
+        // The boxes in the dS^T tile go to the TMA first: the next phase B waits for them,
+        // while the dO stage is only needed again two blocks later.
+        bool go = true;
+        if (wq < 2) go = mbar_wait(&bars->sds_free, n & 1, abort_flag, p.err, p.wait_ns);
+        if (go && q0 < p.N) {
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_3d(&mdq, st + cc * 4096, 32 * cc, q0, u.bh);
           bulk_commit_group();
