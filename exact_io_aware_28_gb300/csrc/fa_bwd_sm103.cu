@@ -309,16 +309,14 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) << 5) << 16);
     const float c = p.scale * kLog2e;
     const size_t row_off = static_cast<size_t>(u.bh) * p.N;
-    float st_l2 = INFINITY, st_dd = 0.f;
+    // Raw lse and D of one column of the next block, loaded a block ahead; they are only
+    // transformed when written to shared memory, so the loads never stall this block.
+    float st_lse = -INFINITY, st_dd = 0.f;
     auto load_stats = [&](int iq) {
-      st_l2 = INFINITY;
-      st_dd = 0.f;
       const int qrow = iq * kBlk + 64 * w + r;
-      if (iq >= 0 && qrow < p.N) {
-        const float lv = lse[row_off + qrow];
-        st_l2 = lv == -INFINITY ? INFINITY : lv * kLog2e;
-        st_dd = Dsum[row_off + qrow];
-      }
+      const bool in = iq >= 0 && qrow < p.N;
+      st_lse = in ? lse[row_off + qrow] : -INFINITY;
+      st_dd = in ? Dsum[row_off + qrow] : 0.f;
     };
     if (r < 64) load_stats(first);
     bool ok = true;
@@ -334,7 +332,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       // outside the sequence or sees no key, so that P = 0 there) and D.  They were loaded
       // into registers during the previous block; the next block's are requested now.
       if (r < 64) {
-        sL[64 * w + r] = st_l2;
+        sL[64 * w + r] = st_lse == -INFINITY ? INFINITY : st_lse * kLog2e;
         sD[64 * w + r] = st_dd;
         load_stats(next_q(p, u, i));
       }
