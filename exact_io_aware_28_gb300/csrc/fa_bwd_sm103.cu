@@ -124,8 +124,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   uint8_t* sV = sK + C::TILE;
   uint8_t* sQ = sV + C::TILE;                  // [NSTAGE][Q tile, dO tile]
   uint8_t* sDS = sQ + C::NSTAGE * 2 * C::TILE;
-  float* sL = reinterpret_cast<float*>(sDS + C::DS);   // [128] lse * log2(e) (or +inf)
-  float* sD = sL + kBlk;                               // [128] D
+  float* sL = reinterpret_cast<float*>(sDS + C::DS);   // [128] -lse * log2(e) (or -inf)
+  float* sD = sL + kBlk;                               // [128] -D
   Bars* bars = reinterpret_cast<Bars*>(sD + kBlk);
   volatile int* abort_flag = &bars->abort;
 
@@ -328,12 +328,13 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         ok = mbar_wait_warp(&bars->ds_ready, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
         if (!ok) break;
       }
-      // Column statistics of this query block: lse * log2(e) (+inf where the row is
-      // outside the sequence or sees no key, so that P = 0 there) and D.  They were loaded
+      // Column statistics of this query block, negated for packed fma/add: -lse * log2(e)
+      // (-inf where the row is outside the sequence or sees no key, so that P = 0 there)
+      // and -D.  They were loaded
       // into registers during the previous block; the next block's are requested now.
       if (r < 64) {
-        sL[64 * w + r] = st_lse == -INFINITY ? INFINITY : st_lse * kLog2e;
-        sD[64 * w + r] = st_dd;
+        sL[64 * w + r] = st_lse == -INFINITY ? -INFINITY : -st_lse * kLog2e;
+        sD[64 * w + r] = -st_dd;
         load_stats(next_q(p, u, i));
       }
       mbar_arrive(&bars->stats_full);
@@ -346,6 +347,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       if (!ok) break;
       tc_fence_after();
       uint32_t pp[32];
+      const uint64_t c2 = f2_pack(c, c);
       // Off the diagonal, every query column of a live key row is visible: no masks.
       const bool masked = diag || !key_live;
 #pragma unroll
@@ -353,17 +355,21 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         uint32_t sv[32];
         tmem_ld32_wait(lane_base + 64 * w + 32 * h, sv);
         const float* L = sL + 64 * w + 32 * h;
+        const float2* L2 = reinterpret_cast<const float2*>(L);
         if (!masked) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            pp[16 * h + e / 2] = pack_bf16x2(ex2(fmaf(__uint_as_float(sv[e]), c, -L[e])),
-                                             ex2(fmaf(__uint_as_float(sv[e + 1]), c, -L[e + 1])));
+          for (int e = 0; e < 32; e += 2) {
+            const float2 l = L2[e / 2];
+            const float2 x = f2_unpack(ffma2(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                             c2, f2_pack(l.x, l.y)));
+            pp[16 * h + e / 2] = pack_bf16x2(ex2(x.x), ex2(x.y));
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int q0 = 64 * w + 32 * h + e;
-            float pa = ex2(fmaf(__uint_as_float(sv[e]), c, -L[e]));
-            float pb = ex2(fmaf(__uint_as_float(sv[e + 1]), c, -L[e + 1]));
+            float pa = ex2(fmaf(__uint_as_float(sv[e]), c, L[e]));
+            float pb = ex2(fmaf(__uint_as_float(sv[e + 1]), c, L[e + 1]));
             if (!key_live || q0 < lim) pa = 0.f;
             if (!key_live || q0 + 1 < lim) pb = 0.f;
             pp[16 * h + e / 2] = pack_bf16x2(pa, pb);
@@ -388,13 +394,15 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         const float4* D4 = reinterpret_cast<const float4*>(sD + 64 * w + 32 * h);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 dd = D4[e4];
+          const float4 nd = D4[e4];   // -D
           const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * h + 2 * e4]));
           const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * h + 2 * e4 + 1]));
-          dsp[2 * e4] = pack_bf16x2(p01.x * (__uint_as_float(dpv[4 * e4 + 0]) - dd.x),
-                                    p01.y * (__uint_as_float(dpv[4 * e4 + 1]) - dd.y));
-          dsp[2 * e4 + 1] = pack_bf16x2(p23.x * (__uint_as_float(dpv[4 * e4 + 2]) - dd.z),
-                                        p23.y * (__uint_as_float(dpv[4 * e4 + 3]) - dd.w));
+          const float2 d01 = f2_unpack(fmul2(f2_pack(p01.x, p01.y),
+              fadd2(f2_pack(__uint_as_float(dpv[4 * e4 + 0]), __uint_as_float(dpv[4 * e4 + 1])), f2_pack(nd.x, nd.y))));
+          const float2 d23 = f2_unpack(fmul2(f2_pack(p23.x, p23.y),
+              fadd2(f2_pack(__uint_as_float(dpv[4 * e4 + 2]), __uint_as_float(dpv[4 * e4 + 3])), f2_pack(nd.z, nd.w))));
+          dsp[2 * e4] = pack_bf16x2(d01.x, d01.y);
+          dsp[2 * e4 + 1] = pack_bf16x2(d23.x, d23.y);
         }
         // dS^T over this warpgroup's already-read dP^T columns, and into the swizzled
         // shared tile (row r, query columns 64w + 32h ...).

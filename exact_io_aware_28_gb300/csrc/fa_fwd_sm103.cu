@@ -309,35 +309,40 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+      float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int i = 4; i < 128; i += 4) {
-        mx0 = fmaxf(mx0, s[i]);
-        mx1 = fmaxf(mx1, s[i + 1]);
-        mx2 = fmaxf(mx2, s[i + 2]);
-        mx3 = fmaxf(mx3, s[i + 3]);
+      for (int i = 8; i < 128; i += 8) {
+        mx0 = fmax3(mx0, s[i], s[i + 1]);
+        mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+        mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+        mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
       }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float mt = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * c;
       float m_new = m_run;
       if (mt > m_run + kRescaleThreshold) m_new = mt;
       const bool changed = m_new != m_run;
       const float alpha = changed ? ex2(m_run - m_new) : 1.f;  // m_run = -inf gives 0
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      float sum0 = 0.f, sum1 = 0.f;
+      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_use, -m_use);
+      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float a = ex2(fmaf(s[64 * half + 2 * i], c, -m_use));
-          const float b = ex2(fmaf(s[64 * half + 2 * i + 1], c, -m_use));
-          sum0 += a;
-          sum1 += b;
+          const float2 x = f2_unpack(ffma2(f2_pack(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), c2, nm2));
+          const float a = ex2(x.x);
+          const float b = ex2(x.y);
+          if (i & 1) acc1 = fadd2(acc1, f2_pack(a, b));
+          else acc0 = fadd2(acc0, f2_pack(a, b));
           pk[i] = pack_bf16x2(a, b);
         }
         // P overwrites the first 64 columns of this tile's S region (already read).
         tmem_st32(lane_base + s_col + 32 * half, pk);
       }
+      const float2 accs = f2_unpack(fadd2(acc0, acc1));
+      const float sum0 = accs.x, sum1 = accs.y;
       l = l * alpha + (sum0 + sum1);
       m_run = m_new;
       // Rescale the running O (previous P V products have completed: the S MMA this
