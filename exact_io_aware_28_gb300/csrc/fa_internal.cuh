@@ -53,6 +53,9 @@ bool make_head_map(CUtensorMap* map, const void* ptr, int BH, int N, int d);
 // reduce-add; rows beyond N are outside the map.
 bool make_acc_map(CUtensorMap* map, const void* ptr, int BH, int N, int d);
 
+// Device address of the library's error word on the current device (nullptr on failure).
+int* error_word();
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

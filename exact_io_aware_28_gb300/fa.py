@@ -20,7 +20,8 @@ FA_BF16, FA_FP32 = 0, 1
 
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_preprocess", "fa_bwd_main",
-           "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_status_string", "fa_device_error")
+           "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_status_string", "fa_device_error",
+           "fa_selftest_wait_timeout")
 
 # Largest workspace (bytes) fa_bwd_noalloc can serve from its built-in scratch array.
 FA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -63,6 +64,8 @@ def load() -> ctypes.CDLL:
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_device_error.argtypes = [P]
     lib.fa_device_error.restype = I
+    lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
+    lib.fa_selftest_wait_timeout.restype = I
     _lib = lib
     return lib
 
@@ -103,6 +106,13 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def fa_device_error(stream=None) -> int:
     return int(load().fa_device_error(_stream(stream)))
+
+
+def fa_selftest_wait_timeout(limit_ms: int, stream=None) -> None:
+    """Launch the bounded-wait self-test; fa_device_error() then reports FA_ERR_TIMEOUT."""
+    st = load().fa_selftest_wait_timeout(int(limit_ms), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_selftest_wait_timeout")
 
 
 def fa_fwd(q, k, v, o, lse, causal: bool = False, blockmask=None, kv_len=None,

@@ -166,6 +166,16 @@ const char* fa_status_string(fa_status s);
  */
 fa_status fa_device_error(void* stream);
 
+/*
+ * Self-test of failure detection (no counterpart on the pages; for tests and diagnostics).
+ * Launches one warp that waits, with the bounded mbarrier wait the attention kernels use,
+ * on a barrier nothing ever arrives on.  After `limit_ms` milliseconds (1..10000) the wait
+ * gives up and records FA_ERR_TIMEOUT in the device error word, which the next
+ * fa_device_error(stream) returns (and clears).  Uses no TMA and no tensor memory; the
+ * context stays usable.  Returns FA_ERR_INVALID_ARG for a limit out of range.
+ */
+fa_status fa_selftest_wait_timeout(unsigned int limit_ms, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
