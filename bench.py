@@ -290,10 +290,11 @@ def run_ours(args, world, rank, local):
                 if w.dtype == "bf16" else None)
     peak_t = pk["bf16_tflops_sustained"]
     traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    tr_path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     if os.path.exists(tr_path):
         try:
-            traffic = json.load(open(tr_path)).get(args.workload, {}).get("bwd_main")
+            if not args.heads:
+                traffic = json.load(open(tr_path)).get(args.workload, {}).get("bwd_main")
         except ValueError:
             traffic = None
     roofline = {"kernel": "bwd main (dK, dV, dQ partials)", "bound": "tensor",
