@@ -469,18 +469,26 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       const int q0 = i * kBlk + 32 * wq;
       uint8_t* st = wq < 2 ? sQ + (n & 1) * 2 * C::TILE + C::TILE + wq * (D / 32) * 4096
                            : sDS + (wq - 2) * (D / 32) * 4096;
+      // Two 32-column chunks per TMEM round trip; the columns are released as soon as the
+      // last chunk is in registers, before its shared-memory stores.
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld32_wait(lane_base + 128 + cc * 32, v);
-        uint8_t* row = st + cc * 4096 + lane * 128;
+      for (int c2 = 0; c2 < D / 64; ++c2) {
+        uint32_t v[64];
+        tmem_ld64_wait(lane_base + 128 + c2 * 64, lane_base + 128 + c2 * 64 + 32, v);
+        if (c2 == D / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(&bars->dq_free);
+        }
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
-              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int h = 0; h < 2; ++h) {
+          uint8_t* row = st + (2 * c2 + h) * 4096 + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(v[32 * h + 4 * j], v[32 * h + 4 * j + 1], v[32 * h + 4 * j + 2],
+                           v[32 * h + 4 * j + 3]);
+        }
       }
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
