@@ -185,92 +185,97 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread.  tcgen05.mma returns only once the tensor pipe takes the instruction, so
+    // this thread runs in step with the pipe: everything it does between two groups of
+    // MMAs is a bubble.  The loop therefore waits for V_j and K_{j+1} together, before the
+    // first group of the step, and each softmax handshake is the only wait in front of its
+    // P V group.  Descriptors are built once and advanced by adding (offset >> 4) to the
+    // 14-bit start-address field.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
-      const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
-      int last[2] = {-1, -1};
-      for (int j = 0; j < jend; ++j)
-        for (int t = 0; t < 2; ++t)
-          if (need(p, u, t, j)) last[t] = j;
-      int cs = 0, cr = 0;           // ring position consumed
-      int npv[2] = {0, 0};
+      constexpr uint64_t kTileD = C::TILE >> 4;
+      const uint64_t dQ = sw128_desc(smem_u32(sQ), 16, 1024);      // K-major Q tiles
+      const uint64_t dK = sw128_desc(smem_u32(sKV), 16, 1024);     // K-major K stages
+      const uint64_t dV = sw128_desc(smem_u32(sKV), kSub, 1024);   // MN-major V stages
+      int last0 = -1, last1 = -1;
+      for (int j = jend - 1; j >= 0 && (last0 < 0 || last1 < 0); --j) {
+        if (last0 < 0 && need(p, u, 0, j)) last0 = j;
+        if (last1 < 0 && need(p, u, 1, j)) last1 = j;
+      }
+      int cs = 0;
+      uint32_t cr = 0;  // ring slot and the parity of its current fill
+      int npv0 = 0, npv1 = 0;
       bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
-      auto issue_s = [&](int t, uint32_t kaddr) {
-        const uint32_t qaddr = sQa + t * C::TILE;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
-          mma_ss(tb + t * 128, sw128_desc(qaddr + off, 16, 1024), sw128_desc(kaddr + off, 16, 1024),
-                 idS, kk > 0);
-        }
-        mma_commit(&bars->s_full[t]);
-      };
-      auto issue_pv = [&](int t, uint32_t vaddr) {
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tb + 256 + t * 128, tb + t * 128 + 8 * kk,
-                 sw128_desc(vaddr + 2048 * kk, kSub, 1024), idO, (npv[t] > 0 || kk > 0) ? 1u : 0u);
-        ++npv[t];
-      };
-      auto wait_full = [&]() -> bool {
-        const bool r = mbar_wait(&bars->kv_full[cs], cr & 1, abort_flag, p.err, p.wait_ns);
-        tc_fence_after();
-        return r;
-      };
-      auto advance = [&]() {
-        if (++cs == C::NSTAGE) {
-          cs = 0;
-          ++cr;
-        }
-      };
+#define FA_ISSUE_S(t, slot)                                                                  \
+  do {                                                                                       \
+    _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                  \
+      const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kSub + (kk & 3) * 32) >> 4);   \
+      mma_ss(tb + (t) * 128, dQ + (t) * kTileD + off, dK + (slot) * kTileD + off, idS,       \
+             kk > 0);                                                                        \
+    }                                                                                        \
+    mma_commit(&bars->s_full[t]);                                                            \
+  } while (0)
+#define FA_ISSUE_PV(t, slot, first)                                                          \
+  do {                                                                                       \
+    _Pragma("unroll") for (int kk = 0; kk < kBlk / 16; ++kk)                                 \
+      mma_ts(tb + 256 + (t) * 128, tb + (t) * 128 + 8 * kk,                                  \
+             dV + (slot) * kTileD + static_cast<uint64_t>((2048 * kk) >> 4), idO,            \
+             ((first) && kk == 0) ? 0u : 1u);                                                \
+  } while (0)
       int j = next_any(p, u, -1, jend);
       if (ok && j >= 0) {
-        ok = wait_full();
+        const int ks = cs;
+        ok = mbar_wait(&bars->kv_full[ks], cr & 1, abort_flag, p.err, p.wait_ns);
+        if (++cs == C::NSTAGE) { cs = 0; ++cr; }
+        tc_fence_after();
         if (ok) {
-          const uint32_t kaddr = sKVa + cs * C::TILE;
-          for (int t = 0; t < 2; ++t)
-            if (need(p, u, t, j)) issue_s(t, kaddr);
-          mma_commit(&bars->kv_empty[cs]);
-          advance();
+          if (need(p, u, 0, j)) FA_ISSUE_S(0, ks);
+          if (need(p, u, 1, j)) FA_ISSUE_S(1, ks);
+          mma_commit(&bars->kv_empty[ks]);
         }
       }
       while (ok && j >= 0) {
         const int jn = next_any(p, u, j, jend);
-        ok = wait_full();  // V_j
-        if (!ok) break;
+        // V_j, then K of the next key block: the producer loads them in this order.
         const int vs = cs;
-        const uint32_t vaddr = sKVa + vs * C::TILE;
-        advance();
+        ok = mbar_wait(&bars->kv_full[vs], cr & 1, abort_flag, p.err, p.wait_ns);
+        if (++cs == C::NSTAGE) { cs = 0; ++cr; }
         int ks = -1;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (need(p, u, t, j)) {
-            ok = mbar_wait(&bars->p_full[t], (npv[t] & 1), abort_flag, p.err, p.wait_ns);
-            tc_fence_after();
-            if (!ok) break;
-            issue_pv(t, vaddr);
-            if (j == last[t]) mma_commit(&bars->o_done[t]);
-          }
-          if (t == 0) {
-            // K of the next key block follows V_j in the ring.
-            if (jn >= 0) {
-              ok = wait_full();
-              if (!ok) break;
-              ks = cs;
-              advance();
-              if (need(p, u, 0, jn)) issue_s(0, sKVa + ks * C::TILE);
-            }
-          }
+        if (ok && jn >= 0) {
+          ks = cs;
+          ok = mbar_wait(&bars->kv_full[ks], cr & 1, abort_flag, p.err, p.wait_ns);
+          if (++cs == C::NSTAGE) { cs = 0; ++cr; }
         }
         if (!ok) break;
+        tc_fence_after();
+        if (need(p, u, 0, j)) {
+          ok = mbar_wait(&bars->p_full[0], npv0 & 1, abort_flag, p.err, p.wait_ns);
+          tc_fence_after();
+          if (!ok) break;
+          FA_ISSUE_PV(0, vs, npv0 == 0);
+          ++npv0;
+          if (j == last0) mma_commit(&bars->o_done[0]);
+        }
+        if (jn >= 0 && need(p, u, 0, jn)) FA_ISSUE_S(0, ks);
+        if (need(p, u, 1, j)) {
+          ok = mbar_wait(&bars->p_full[1], npv1 & 1, abort_flag, p.err, p.wait_ns);
+          tc_fence_after();
+          if (!ok) break;
+          FA_ISSUE_PV(1, vs, npv1 == 0);
+          ++npv1;
+          if (j == last1) mma_commit(&bars->o_done[1]);
+        }
         mma_commit(&bars->kv_empty[vs]);
         if (jn >= 0) {
-          if (need(p, u, 1, jn)) issue_s(1, sKVa + ks * C::TILE);
+          if (need(p, u, 1, jn)) FA_ISSUE_S(1, ks);
           mma_commit(&bars->kv_empty[ks]);
         }
         j = jn;
       }
+#undef FA_ISSUE_S
+#undef FA_ISSUE_PV
       // Drain: every MMA issued above has completed before tensor memory is released.
       mma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, &bars->never, nullptr, p.wait_ns);
