@@ -133,14 +133,14 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], kBlk);
+      mbar_init(&bars->p_full[t], 2 * kBlk);
       mbar_init(&bars->o_done[t], 1);
     }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);
     bars->abort = 0;
     bars->never = 0;
     fence_mbar_init();
@@ -183,46 +183,41 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // One thread.  tcgen05.mma returns only once the tensor pipe takes the instruction, so
-    // this thread runs in step with the pipe: everything it does between two groups of
-    // MMAs is a bubble.  The loop therefore waits for V_j and K_{j+1} together, before the
-    // first group of the step, and each softmax handshake is the only wait in front of its
-    // P V group.  Descriptors are built once and advanced by adding (offset >> 4) to the
-    // 14-bit start-address field.
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread per query tile: warp 1 issues tile 0's MMAs, warp 3 tile 1's.
+    // tcgen05.mma returns only once the tensor pipe takes the instruction, so a single
+    // issuer runs in step with the pipe and every wait it makes between two groups is a
+    // bubble; with one issuer per tile the pipe takes the other tile's MMAs meanwhile.
+    // Each issuer walks the whole K/V ring (both tiles release every slot, so kv_empty
+    // counts two arrivals) and, per key block j, issues O_t += P_t V_j after its softmax
+    // handshake, then S_t = Q_t K_{j+1}^T.  In-order execution of one thread's MMAs keeps
+    // S_t(j+1) from overwriting P_t(j) before the P V product has read it.  Descriptors
+    // are built once and advanced by adding (offset >> 4) to the start-address field.
     if (lane == 0) {
+      const int t = warp == 1 ? 0 : 1;
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
       constexpr uint64_t kTileD = C::TILE >> 4;
-      const uint64_t dQ = sw128_desc(smem_u32(sQ), 16, 1024);      // K-major Q tiles
+      const uint64_t dQ = sw128_desc(smem_u32(sQ + t * C::TILE), 16, 1024);  // K-major Q_t
       const uint64_t dK = sw128_desc(smem_u32(sKV), 16, 1024);     // K-major K stages
       const uint64_t dV = sw128_desc(smem_u32(sKV), kSub, 1024);   // MN-major V stages
-      int last0 = -1, last1 = -1;
-      for (int j = jend - 1; j >= 0 && (last0 < 0 || last1 < 0); --j) {
-        if (last0 < 0 && need(p, u, 0, j)) last0 = j;
-        if (last1 < 0 && need(p, u, 1, j)) last1 = j;
-      }
+      const uint32_t tS = tb + t * 128, tO = tb + 256 + t * 128;
+      int last = -1;
+      for (int j = jend - 1; j >= 0 && last < 0; --j)
+        if (need(p, u, t, j)) last = j;
       int cs = 0;
       uint32_t cr = 0;  // ring slot and the parity of its current fill
-      int npv0 = 0, npv1 = 0;
+      int npv = 0;
       bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
-#define FA_ISSUE_S(t, slot)                                                                  \
+#define FA_ISSUE_S(slot)                                                                     \
   do {                                                                                       \
     _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                  \
       const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kSub + (kk & 3) * 32) >> 4);   \
-      mma_ss(tb + (t) * 128, dQ + (t) * kTileD + off, dK + (slot) * kTileD + off, idS,       \
-             kk > 0);                                                                        \
+      mma_ss(tS, dQ + off, dK + (slot) * kTileD + off, idS, kk > 0);                         \
     }                                                                                        \
     mma_commit(&bars->s_full[t]);                                                            \
-  } while (0)
-#define FA_ISSUE_PV(t, slot, first)                                                          \
-  do {                                                                                       \
-    _Pragma("unroll") for (int kk = 0; kk < kBlk / 16; ++kk)                                 \
-      mma_ts(tb + 256 + (t) * 128, tb + (t) * 128 + 8 * kk,                                  \
-             dV + (slot) * kTileD + static_cast<uint64_t>((2048 * kk) >> 4), idO,            \
-             ((first) && kk == 0) ? 0u : 1u);                                                \
   } while (0)
       int j = next_any(p, u, -1, jend);
       if (ok && j >= 0) {
@@ -231,8 +226,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         if (++cs == C::NSTAGE) { cs = 0; ++cr; }
         tc_fence_after();
         if (ok) {
-          if (need(p, u, 0, j)) FA_ISSUE_S(0, ks);
-          if (need(p, u, 1, j)) FA_ISSUE_S(1, ks);
+          if (need(p, u, t, j)) FA_ISSUE_S(ks);
           mma_commit(&bars->kv_empty[ks]);
         }
       }
@@ -250,156 +244,182 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
         if (!ok) break;
         tc_fence_after();
-        if (need(p, u, 0, j)) {
-          ok = mbar_wait(&bars->p_full[0], npv0 & 1, abort_flag, p.err, p.wait_ns);
+        if (need(p, u, t, j)) {
+          ok = mbar_wait(&bars->p_full[t], npv & 1, abort_flag, p.err, p.wait_ns);
           tc_fence_after();
           if (!ok) break;
-          FA_ISSUE_PV(0, vs, npv0 == 0);
-          ++npv0;
-          if (j == last0) mma_commit(&bars->o_done[0]);
-        }
-        if (jn >= 0 && need(p, u, 0, jn)) FA_ISSUE_S(0, ks);
-        if (need(p, u, 1, j)) {
-          ok = mbar_wait(&bars->p_full[1], npv1 & 1, abort_flag, p.err, p.wait_ns);
-          tc_fence_after();
-          if (!ok) break;
-          FA_ISSUE_PV(1, vs, npv1 == 0);
-          ++npv1;
-          if (j == last1) mma_commit(&bars->o_done[1]);
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tO, tS + 8 * kk, dV + vs * kTileD + static_cast<uint64_t>((2048 * kk) >> 4),
+                   idO, (npv > 0 || kk > 0) ? 1u : 0u);
+          ++npv;
+          if (j == last) mma_commit(&bars->o_done[t]);
         }
         mma_commit(&bars->kv_empty[vs]);
         if (jn >= 0) {
-          if (need(p, u, 1, jn)) FA_ISSUE_S(1, ks);
+          if (need(p, u, t, jn)) FA_ISSUE_S(ks);
           mma_commit(&bars->kv_empty[ks]);
         }
         j = jn;
       }
 #undef FA_ISSUE_S
-#undef FA_ISSUE_PV
-      // Drain: every MMA issued above has completed before tensor memory is released.
+      // Drain: every MMA issued by either thread has completed before tensor memory is
+      // released (the barrier counts one arrival per issuer).
       mma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, &bars->never, nullptr, p.wait_ns);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax warpgroups
-    const int t = (warp - 4) >> 2;
-    const int r = ((warp & 3) << 5) + lane;
-    const int row = u.q0 + t * kBlk + r;
-    const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) << 5) << 16);
-    const uint32_t s_col = t * 128;
-    const uint32_t o_col = 256 + t * 128;
+    // ------------------------------------------------------------ softmax warps
+    // All eight warps work on each tile in turn (tile 0 then tile 1 for every key block),
+    // so a tile's softmax runs on two warps per SM sub-partition.  Warp 4 + q + 4h owns
+    // rows 32q + 16h + [0, 16) of both tiles through the 16-lane TMEM shapes: thread t holds
+    // rows A = 32q + 16h + t/4 and B = A + 8, keys 8c + 2(t%4) + {0, 1} for c = 0..15.  The
+    // four threads of a row combine their row maxima with two shuffles; row sums stay
+    // partial per thread until the epilogue.
+    const int q4 = warp & 3, h = (warp - 4) >> 2, t4 = lane & 3;
+    const int rA = 32 * q4 + 16 * h + (lane >> 2), rB = rA + 8;   // rows within a tile
+    const uint32_t lane_base = tb + (static_cast<uint32_t>(32 * q4 + 16 * h) << 16);
     const float c = p.scale * kLog2e;
-    float m_run = -INFINITY, l = 0.f;
-    int n = 0;
+    const uint64_t c2 = f2_pack(c, c);
+    float m_run[2][2] = {{-INFINITY, -INFINITY}, {-INFINITY, -INFINITY}};  // [tile][A/B]
+    float l_part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    int n_t[2] = {0, 0};
     bool ok = true;
     for (int j = 0; j < jend && ok; ++j) {
-      if (!need(p, u, t, j)) continue;
-      ok = mbar_wait_warp(&bars->s_full[t], n & 1, abort_flag, p.err, p.wait_ns);
-      if (!ok) break;
-      tc_fence_after();
-      float s[128];
-      {
-        uint32_t v[128];
-        tmem_ld128_wait(lane_base + s_col, v);
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(v[i]);
-      }
-      const int k0 = j * kBlk;
-      const bool edge = (p.causal && k0 + kBlk - 1 > u.q0 + t * kBlk) || (k0 + kBlk > u.L);
-      if (edge) {
-        const int lim_causal = p.causal ? row - k0 : kBlk - 1;     // last visible column
-        const int lim_len = u.L - 1 - k0;
-        const int lim = min(lim_causal, lim_len);
+      for (int t = 0; t < 2; ++t) {
+        if (!ok || !need(p, u, t, j)) continue;
+        ok = mbar_wait_warp(&bars->s_full[t], n_t[t] & 1, abort_flag, p.err, p.wait_ns);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t v[64];
+        tmem_ld_16x256b_x16_wait(lane_base + t * 128, v);
+        float sv[64];
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i > lim) s[i] = -INFINITY;
-      }
-      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
-      float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
+        for (int i = 0; i < 64; ++i) sv[i] = __uint_as_float(v[i]);
+        const int k0 = j * kBlk;
+        const int row0 = u.q0 + t * kBlk;
+        const bool edge = (p.causal && k0 + kBlk - 1 > row0) || (k0 + kBlk > u.L);
+        if (edge) {
+          const int lim_len = u.L - 1 - k0;
+          const int limA = min(p.causal ? row0 + rA - k0 : kBlk - 1, lim_len);
+          const int limB = min(p.causal ? row0 + rB - k0 : kBlk - 1, lim_len);
 #pragma unroll
-      for (int i = 8; i < 128; i += 8) {
-        mx0 = fmax3(mx0, s[i], s[i + 1]);
-        mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
-        mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
-        mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
-      }
-      const float mt = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * c;
-      float m_new = m_run;
-      if (mt > m_run + kRescaleThreshold) m_new = mt;
-      const bool changed = m_new != m_run;
-      const float alpha = changed ? ex2(m_run - m_new) : 1.f;  // m_run = -inf gives 0
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_use, -m_use);
-      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 x = f2_unpack(ffma2(f2_pack(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), c2, nm2));
-          const float a = ex2(x.x);
-          const float b = ex2(x.y);
-          if (i & 1) acc1 = fadd2(acc1, f2_pack(a, b));
-          else acc0 = fadd2(acc0, f2_pack(a, b));
-          pk[i] = pack_bf16x2(a, b);
-        }
-        // P overwrites the first 64 columns of this tile's S region (already read).
-        tmem_st32(lane_base + s_col + 32 * half, pk);
-      }
-      const float2 accs = f2_unpack(fadd2(acc0, acc1));
-      const float sum0 = accs.x, sum1 = accs.y;
-      l = l * alpha + (sum0 + sum1);
-      m_run = m_new;
-      // Rescale the running O (previous P V products have completed: the S MMA this
-      // warpgroup just waited for was issued after them).
-      if (n > 0 && __any_sync(0xffffffffu, changed)) {
-#pragma unroll
-        for (int cchunk = 0; cchunk < D / 32; ++cchunk) {
-          uint32_t v[32];
-          tmem_ld32_wait(lane_base + o_col + cchunk * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(lane_base + o_col + cchunk * 32, v);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[t]);
-      ++n;
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && n > 0) {
-      ok = mbar_wait_warp(&bars->o_done[t], 0, abort_flag, p.err, p.wait_ns);
-      tc_fence_after();
-    }
-    if (ok) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool store = row < p.N;
-      __nv_bfloat16* orow = o + (static_cast<size_t>(u.bh) * p.N + row) * D;
-#pragma unroll
-      for (int cchunk = 0; cchunk < D / 32; ++cchunk) {
-        uint32_t v[32];
-        if (n > 0) {
-          tmem_ld32_wait(lane_base + o_col + cchunk * 32, v);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        if (store) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]) * inv, __uint_as_float(v[8 * g + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]) * inv, __uint_as_float(v[8 * g + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]) * inv, __uint_as_float(v[8 * g + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]) * inv, __uint_as_float(v[8 * g + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + cchunk * 32 + 8 * g) = w;
+          for (int cc = 0; cc < 16; ++cc) {
+            const int key = 8 * cc + 2 * t4;
+            if (key > limA) sv[4 * cc] = -INFINITY;
+            if (key + 1 > limA) sv[4 * cc + 1] = -INFINITY;
+            if (key > limB) sv[4 * cc + 2] = -INFINITY;
+            if (key + 1 > limB) sv[4 * cc + 3] = -INFINITY;
           }
         }
+        float ma0 = fmaxf(sv[0], sv[1]), ma1 = fmaxf(sv[4], sv[5]);
+        float mb0 = fmaxf(sv[2], sv[3]), mb1 = fmaxf(sv[6], sv[7]);
+#pragma unroll
+        for (int cc = 2; cc < 16; cc += 2) {
+          ma0 = fmax3(ma0, sv[4 * cc], sv[4 * cc + 1]);
+          mb0 = fmax3(mb0, sv[4 * cc + 2], sv[4 * cc + 3]);
+          ma1 = fmax3(ma1, sv[4 * cc + 4], sv[4 * cc + 5]);
+          mb1 = fmax3(mb1, sv[4 * cc + 6], sv[4 * cc + 7]);
+        }
+        float mA = fmaxf(ma0, ma1), mB = fmaxf(mb0, mb1);
+        mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, 1));
+        mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, 1));
+        mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, 2));
+        mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, 2));
+        mA *= c;
+        mB *= c;
+        const float oldA = m_run[t][0], oldB = m_run[t][1];
+        const float newA = mA > oldA + kRescaleThreshold ? mA : oldA;
+        const float newB = mB > oldB + kRescaleThreshold ? mB : oldB;
+        const bool chA = newA != oldA, chB = newB != oldB;
+        const float alphaA = chA ? ex2(oldA - newA) : 1.f;  // old = -inf gives 0
+        const float alphaB = chB ? ex2(oldB - newB) : 1.f;
+        const float useA = newA == -INFINITY ? 0.f : newA;
+        const float useB = newB == -INFINITY ? 0.f : newB;
+        const uint64_t nA = f2_pack(-useA, -useA), nB = f2_pack(-useB, -useB);
+        uint64_t accA = f2_pack(0.f, 0.f), accB = accA;
+        uint32_t pk[32];
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const float2 xa = f2_unpack(ffma2(f2_pack(sv[4 * cc], sv[4 * cc + 1]), c2, nA));
+          const float2 xb = f2_unpack(ffma2(f2_pack(sv[4 * cc + 2], sv[4 * cc + 3]), c2, nB));
+          const float pa0 = ex2(xa.x), pa1 = ex2(xa.y);
+          const float pb0 = ex2(xb.x), pb1 = ex2(xb.y);
+          accA = fadd2(accA, f2_pack(pa0, pa1));
+          accB = fadd2(accB, f2_pack(pb0, pb1));
+          pk[2 * cc] = pack_bf16x2(pa0, pa1);
+          pk[2 * cc + 1] = pack_bf16x2(pb0, pb1);
+        }
+        // P (bf16 pairs) overwrites the first 64 columns of this tile's S region in this
+        // warp's 16 lanes, which no other warp reads; the load above has completed.
+        tmem_st_16x128b_x16(lane_base + t * 128, pk);
+        const float2 sa = f2_unpack(accA), sb = f2_unpack(accB);
+        l_part[t][0] = l_part[t][0] * alphaA + (sa.x + sa.y);
+        l_part[t][1] = l_part[t][1] * alphaB + (sb.x + sb.y);
+        m_run[t][0] = newA;
+        m_run[t][1] = newB;
+        // Rescale the running O (the P V products issued before the S just read are done).
+        if (n_t[t] > 0 && __any_sync(0xffffffffu, chA || chB)) {
+#pragma unroll
+          for (int half = 0; half < D / 64; ++half) {
+            uint32_t o[32];
+            const uint32_t oaddr = lane_base + 256 + t * 128 + 64 * half;
+            tmem_ld_16x256b_x8_wait(oaddr, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * ((i & 2) ? alphaB : alphaA));
+            tmem_st_16x256b_x8(oaddr, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[t]);
+        ++n_t[t];
       }
-      if (store)
-        lse[static_cast<size_t>(u.bh) * p.N + row] =
-            l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
+    }
+    // ------------------------------------------------------------ epilogue
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (ok && n_t[t] > 0) {
+        ok = mbar_wait_warp(&bars->o_done[t], 0, abort_flag, p.err, p.wait_ns);
+        tc_fence_after();
+      }
+      if (!ok) break;
+      float lA = l_part[t][0], lB = l_part[t][1];
+      lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+      lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+      lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+      lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+      const float invA = lA > 0.f ? 1.f / lA : 0.f, invB = lB > 0.f ? 1.f / lB : 0.f;
+      const int rowA = u.q0 + t * kBlk + rA, rowB = rowA + 8;
+      __nv_bfloat16* oA = o + (static_cast<size_t>(u.bh) * p.N + rowA) * D;
+      __nv_bfloat16* oB = oA + 8 * D;
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t ov[32];
+        if (n_t[t] > 0) {
+          tmem_ld_16x256b_x8_wait(lane_base + 256 + t * 128 + 64 * half, ov);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = 0u;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const int col = 64 * half + 8 * cc + 2 * t4;
+          if (rowA < p.N)
+            *reinterpret_cast<uint32_t*>(oA + col) =
+                pack_bf16x2(__uint_as_float(ov[4 * cc]) * invA, __uint_as_float(ov[4 * cc + 1]) * invA);
+          if (rowB < p.N)
+            *reinterpret_cast<uint32_t*>(oB + col) =
+                pack_bf16x2(__uint_as_float(ov[4 * cc + 2]) * invB, __uint_as_float(ov[4 * cc + 3]) * invB);
+        }
+      }
+      if (t4 == 0) {
+        float* lrow = lse + static_cast<size_t>(u.bh) * p.N;
+        if (rowA < p.N) lrow[rowA] = lA > 0.f ? (m_run[t][0] + __log2f(lA)) * kLn2 : -INFINITY;
+        if (rowB < p.N) lrow[rowB] = lB > 0.f ? (m_run[t][1] + __log2f(lB)) * kLn2 : -INFINITY;
+      }
     }
   }
 
