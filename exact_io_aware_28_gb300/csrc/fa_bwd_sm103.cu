@@ -20,16 +20,15 @@
 //   dP^T = V_j dO_i^T  (A: V_j K-major smem,    B: dO_i K-major smem)   -> TMEM [128,256)
 //   dV  += P^T dO_i    (A: P^T bf16 in TMEM,    B: dO_i MN-major smem)  -> TMEM [256,256+d)
 //   dK  += dS^T Q_i    (A: dS^T bf16 in TMEM,   B: Q_i MN-major smem)   -> TMEM [384,384+d)
-//   d = 128: dQ_i^T = K_j^T dS^T (A: K_j MN-major smem, B: dS^T MN-major smem) -> TMEM [128,256)
-//   d = 64:  dQ_i   = dS K_j     (A: dS^T MN-major smem, B: K_j MN-major smem) -> TMEM [128,192)
-// P^T is written over already-read S^T columns, dS^T over already-read dP^T columns.
-// Warps (16): 0-3 the dQ drain, 4-7 and 8-11
-// two warpgroups that each take 64 of the 128 query columns of every key row (phase A: P^T
-// from S^T; phase B: dS^T from dP^T), 12 TMA producer (K_j, V_j once; Q_i and dO_i through
-// two-stage rings) and tensor-memory allocation, 13 MMA issuer, 14-15 idle.  With d = 128 the partial is produced transposed (TMEM lane = head dimension),
-// so each warp's atomics cover 32 consecutive floats of one accumulator row (one 128-byte
-// segment) instead of touching 32 rows; with d = 64 one thread per query row adds 16-byte
-// vectors.
+//   dQ_i = dS K_j      (A: dS^T MN-major smem,  B: K_j MN-major smem)   -> TMEM [128,128+d)
+// P^T is written over already-read S^T columns, dS^T over already-read dP^T columns, and
+// dQ_i (TMEM lane = query row) over the dP^T region once dK has read dS^T.
+// Warps (16): 0-3 the dQ drain, 4-7 and 8-11 two warpgroups that each take 64 of the 128
+// query columns of every key row (phase A: P^T from S^T; phase B: dS^T from dP^T), 12 TMA
+// producer (K_j, V_j once; Q_i and dO_i through two-stage rings) and tensor-memory
+// allocation, 13 MMA issuer, 14-15 idle.  The drain copies each dQ_i partial out of TMEM
+// into 128-byte-swizzled [32 rows][32 columns] fp32 boxes in shared memory and adds them to
+// the fp32 accumulator in global memory with TMA bulk reduce-adds.
 // MMA issue order per block n: dV(n), S^T(n+1), dK(n), dQ(n), dP^T(n+1).  dP^T(n+1) goes
 // into the columns of dQ(n) as soon as the drain has copied them out, so the next block's
 // phase B can follow its phase A directly; dV(n+1) and S^T(n+2) then run during that
