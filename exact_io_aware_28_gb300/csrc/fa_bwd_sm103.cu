@@ -20,19 +20,19 @@
 //   dP^T = V_j dO_i^T  (A: V_j K-major smem,    B: dO_i K-major smem)   -> TMEM [128,256)
 //   dV  += P^T dO_i    (A: P^T bf16 in TMEM,    B: dO_i MN-major smem)  -> TMEM [256,256+d)
 //   dK  += dS^T Q_i    (A: dS^T bf16 in TMEM,   B: Q_i MN-major smem)   -> TMEM [384,384+d)
-//   dQ_i = dS K_j      (A: dS^T MN-major smem,  B: K_j MN-major smem)   -> TMEM [128,128+d)
-// P^T is written over already-read S^T columns, dS^T over already-read dP^T columns, and
-// dQ_i (TMEM lane = query row) over the dP^T region once dK has read dS^T.
+//   dQ_i = dS K_j      (A: dS^T MN-major smem,  B: K_j MN-major smem)   -> TMEM [0,d)
+// P^T is written over already-read S^T columns and dS^T over already-read dP^T columns;
+// dQ_i (TMEM lane = query row) goes into the S^T region once dV has read P^T.
 // Warps (16): 0-3 the dQ drain, 4-7 and 8-11 two warpgroups that each take 64 of the 128
 // query columns of every key row (phase A: P^T from S^T; phase B: dS^T from dP^T), 12 TMA
 // producer (K_j, V_j once; Q_i and dO_i through two-stage rings) and tensor-memory
 // allocation, 13 MMA issuer, 14-15 idle.  The drain copies each dQ_i partial out of TMEM
 // into 128-byte-swizzled [32 rows][32 columns] fp32 boxes in shared memory and adds them to
 // the fp32 accumulator in global memory with TMA bulk reduce-adds.
-// MMA issue order per block n: dV(n), S^T(n+1), dK(n), dQ(n), dP^T(n+1).  dP^T(n+1) goes
-// into the columns of dQ(n) as soon as the drain has copied them out, so the next block's
-// phase B can follow its phase A directly; dV(n+1) and S^T(n+2) then run during that
-// phase B, dK(n+1) and dQ(n+1) during the following phase A.
+// MMA issue order per block n: dV(n), dQ(n), dK(n), dP^T(n+1), S^T(n+1).  The dQ drain
+// and the bulk reduce-adds behind it decide when the next phase B may reuse the dS tile,
+// so dQ(n) goes first once phase B(n) is done; dP^T(n+1) needs only dK(n) to have read
+// dS^T(n), and S^T(n+1) waits for the drain to have copied dQ(n) out of its columns.
 // Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and exits.
 #include <cuda.h>
 #include <math.h>
@@ -260,38 +260,38 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         for (int kk = 0; kk < kBlk / 16; ++kk)
           mma_ts(tb + 256, tb + a_col(0, kk), sw128_desc(aDO + 2048 * kk, kSub, 1024), idKN,
                  (n > 0 || kk > 0) ? 1u : 0u);
-        // S^T of the next block (its Q tile sits in the other stage of the ring).
-        if (in >= 0) {
-          ok = mbar_wait(&bars->q_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
-                         p.wait_ns);
-          tc_fence_after();
-          if (!ok) break;
-          issue_s(n + 1);
-        }
-        // dK += dS^T Q_i ; dQ_i = dS K_j
+        // dQ_i = dS K_j first, into the S^T columns (P^T has been read by dV above): the dQ
+        // drain and the TMA reduce-adds behind it gate the next phase B, so they start as
+        // early as possible.
         ok = mbar_wait(&bars->ds_ready, n & 1, abort_flag, p.err, p.wait_ns);
         tc_fence_after();
         if (!ok) break;
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tb + 384, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024), idKN,
-                 (n > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tb + 128, sw128_desc(aDS + 2048 * kk, kSub, 1024),
+          mma_ss(tb, sw128_desc(aDS + 2048 * kk, kSub, 1024),
                  sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
         mma_commit(&bars->dq_full);
+        // dK += dS^T Q_i
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ts(tb + 384, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024), idKN,
+                 (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->q_empty[n & 1]);
         mma_commit(&bars->do_empty[n & 1]);
-        // dP^T of the next block, into the columns of dQ(n) as soon as the drain has read
-        // them, so that its phase B can follow its phase A without waiting for dV and S^T.
         if (in >= 0) {
-          ok = mbar_wait(&bars->dq_free, n & 1, abort_flag, p.err, p.wait_ns);
-          ok = ok && mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag,
-                               p.err, p.wait_ns);
+          // dP^T of the next block over dP^T / dS^T of this one (read by phase B and dK).
+          ok = mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
+                         p.wait_ns);
           tc_fence_after();
           if (!ok) break;
           issue_dp(n + 1);
+          // S^T of the next block, once the drain has copied dQ_i out of those columns.
+          ok = mbar_wait(&bars->dq_free, n & 1, abort_flag, p.err, p.wait_ns);
+          ok = ok && mbar_wait(&bars->q_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag,
+                               p.err, p.wait_ns);
+          tc_fence_after();
+          if (!ok) break;
+          issue_s(n + 1);
         }
         i = in;
       }
@@ -473,7 +473,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 #pragma unroll 1
       for (int c2 = 0; c2 < D / 64; ++c2) {
         uint32_t v[64];
-        tmem_ld64_wait(lane_base + 128 + c2 * 64, lane_base + 128 + c2 * 64 + 32, v);
+        tmem_ld64_wait(lane_base + c2 * 64, lane_base + c2 * 64 + 32, v);
         if (c2 == D / 64 - 1) {
           tc_fence_before();
           mbar_arrive(&bars->dq_free);
