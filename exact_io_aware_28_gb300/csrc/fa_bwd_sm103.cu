@@ -29,10 +29,11 @@
 // allocation, 13 MMA issuer, 14-15 idle.  The drain copies each dQ_i partial out of TMEM
 // into 128-byte-swizzled [32 rows][32 columns] fp32 boxes in shared memory and adds them to
 // the fp32 accumulator in global memory with TMA bulk reduce-adds.
-// MMA issue order per block n: dV(n), dQ(n), dK(n), dP^T(n+1), S^T(n+1).  The dQ drain
+// MMA issue order per block n: dV(n), dQ(n), dK(n), S^T(n+1), dP^T(n+1).  The dQ drain
 // and the bulk reduce-adds behind it decide when the next phase B may reuse the dS tile,
-// so dQ(n) goes first once phase B(n) is done; dP^T(n+1) needs only dK(n) to have read
-// dS^T(n), and S^T(n+1) waits for the drain to have copied dQ(n) out of its columns.
+// so dQ(n) goes first once phase B(n) is done; S^T(n+1) follows as soon as the drain has
+// copied dQ(n) out of its columns, so the next phase A starts early; dP^T(n+1) needs only
+// dK(n) to have read dS^T(n).
 // Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and exits.
 #include <cuda.h>
 #include <math.h>
@@ -279,19 +280,20 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         mma_commit(&bars->q_empty[n & 1]);
         mma_commit(&bars->do_empty[n & 1]);
         if (in >= 0) {
-          // dP^T of the next block over dP^T / dS^T of this one (read by phase B and dK).
-          ok = mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
-                         p.wait_ns);
-          tc_fence_after();
-          if (!ok) break;
-          issue_dp(n + 1);
-          // S^T of the next block, once the drain has copied dQ_i out of those columns.
+          // S^T of the next block as soon as the drain has copied dQ_i out of its columns:
+          // the next phase A waits for nothing else.
           ok = mbar_wait(&bars->dq_free, n & 1, abort_flag, p.err, p.wait_ns);
           ok = ok && mbar_wait(&bars->q_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag,
                                p.err, p.wait_ns);
           tc_fence_after();
           if (!ok) break;
           issue_s(n + 1);
+          // dP^T of the next block over dP^T / dS^T of this one (read by phase B and dK).
+          ok = mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
+                         p.wait_ns);
+          tc_fence_after();
+          if (!ok) break;
+          issue_dp(n + 1);
         }
         i = in;
       }
