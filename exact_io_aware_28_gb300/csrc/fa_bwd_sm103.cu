@@ -29,11 +29,11 @@
 // allocation, 13 MMA issuer, 14-15 idle.  The drain copies each dQ_i partial out of TMEM
 // into 128-byte-swizzled [32 rows][32 columns] fp32 boxes in shared memory and adds them to
 // the fp32 accumulator in global memory with TMA bulk reduce-adds.
-// MMA issue order per block n: dV(n), dQ(n), dK(n), S^T(n+1), dP^T(n+1).  The dQ drain
+// MMA issue order per block n: dV(n), dQ(n), S^T(n+1), dK(n), dP^T(n+1).  The dQ drain
 // and the bulk reduce-adds behind it decide when the next phase B may reuse the dS tile,
-// so dQ(n) goes first once phase B(n) is done; S^T(n+1) follows as soon as the drain has
-// copied dQ(n) out of its columns, so the next phase A starts early; dP^T(n+1) needs only
-// dK(n) to have read dS^T(n).
+// so dQ(n) goes first once phase B(n) is done; the drain copies the whole partial out of
+// TMEM in one load, and S^T(n+1) follows as soon as it has, so the next phase A starts
+// early; dP^T(n+1) needs only dK(n) to have read dS^T(n).
 // Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and exits.
 #include <cuda.h>
 #include <math.h>
@@ -52,6 +52,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kProducerWarp = 12;  // also allocates tensor memory
 constexpr int kMmaWarp = 13;       // warps 14-15 idle
 constexpr int kThreads = 512;
+constexpr int kRegsDrain = 200;    // warps 0-3 after reallocation (d = 128)
+constexpr int kRegsControl = 56;   // warps 12-15 after reallocation (d = 128)
 
 template <int D>
 struct Cfg {
@@ -178,9 +180,15 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   tc_fence_after();
   const uint32_t tb = bars->tmem_base;
   const int first = next_q(p, u, -1);
+  // Registers (d = 128): launched with 128 per thread (512 threads).  The producer / MMA
+  // warpgroup (warps 12-15) gives 72 of them back and the dQ drain warpgroup (warps 0-3)
+  // takes them, so a drain warp can hold a whole 128-column dQ row slice in registers:
+  // 4 x 32 x (200 + 128 + 128 + 56) = 512 x 128.  With d = 64 a slice fits as launched.
+  static_assert(kThreads == 512 && kRegsDrain + 2 * 128 + kRegsControl == 4 * 128, "register split");
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
+    if constexpr (D == 128) regs_release_to<kRegsControl>();
     if (lane == 0 && first >= 0) {
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mdo);
@@ -211,6 +219,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    if constexpr (D == 128) regs_release_to<kRegsControl>();
     if (lane == 0 && first >= 0) {
       constexpr uint32_t idSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idKN = idesc_bf16(128, D, false, true);     // dV, dK (B MN-major)
@@ -272,13 +281,6 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           mma_ss(tb, sw128_desc(aDS + 2048 * kk, kSub, 1024),
                  sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
         mma_commit(&bars->dq_full);
-        // dK += dS^T Q_i
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tb + 384, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024), idKN,
-                 (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->q_empty[n & 1]);
-        mma_commit(&bars->do_empty[n & 1]);
         if (in >= 0) {
           // S^T of the next block as soon as the drain has copied dQ_i out of its columns:
           // the next phase A waits for nothing else.
@@ -288,6 +290,15 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           tc_fence_after();
           if (!ok) break;
           issue_s(n + 1);
+        }
+        // dK += dS^T Q_i
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ts(tb + 384, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024), idKN,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->q_empty[n & 1]);
+        mma_commit(&bars->do_empty[n & 1]);
+        if (in >= 0) {
           // dP^T of the next block over dP^T / dS^T of this one (read by phase B and dK).
           ok = mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
                          p.wait_ns);
@@ -451,8 +462,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
       }
     }
+  } else if (warp >= 14) {
+    if constexpr (D == 128) regs_release_to<kRegsControl>();  // idle control warps
   } else if (warp < 4) {
     // ------------------------------------------------------------ dQ partials (query rows)
+    if constexpr (D == 128) regs_grow_to<kRegsDrain>();
     const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) << 5) << 16);
     bool ok = true;
     int n = 0;
@@ -470,24 +484,25 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       const int q0 = i * kBlk + 32 * wq;
       uint8_t* st = wq < 2 ? sQ + (n & 1) * 2 * C::TILE + C::TILE + wq * (D / 32) * 4096
                            : sDS + (wq - 2) * (D / 32) * 4096;
-      // Two 32-column chunks per TMEM round trip; the columns are released as soon as the
-      // last chunk is in registers, before its shared-memory stores.
-#pragma unroll 1
-      for (int c2 = 0; c2 < D / 64; ++c2) {
-        uint32_t v[64];
-        tmem_ld64_wait(lane_base + c2 * 64, lane_base + c2 * 64 + 32, v);
-        if (c2 == D / 64 - 1) {
-          tc_fence_before();
-          mbar_arrive(&bars->dq_free);
+      // The whole row slice comes out of TMEM in one load and the columns are released
+      // before any shared-memory store.
+      {
+        uint32_t v[D];
+        if constexpr (D == 128) {
+          tmem_ld128_wait(lane_base, v);
+        } else {
+          tmem_ld64_wait(lane_base, lane_base + 32, v);
         }
+        tc_fence_before();
+        mbar_arrive(&bars->dq_free);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint8_t* row = st + (2 * c2 + h) * 4096 + lane * 128;
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint8_t* row = st + cc * 4096 + lane * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
-                make_uint4(v[32 * h + 4 * j], v[32 * h + 4 * j + 1], v[32 * h + 4 * j + 2],
-                           v[32 * h + 4 * j + 3]);
+                make_uint4(v[32 * cc + 4 * j], v[32 * cc + 4 * j + 1], v[32 * cc + 4 * j + 2],
+                           v[32 * cc + 4 * j + 3]);
         }
       }
       fence_proxy_async_smem();

@@ -96,6 +96,20 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// ------------------------------------------------------------------ register reallocation
+
+// Per-warpgroup register limits.  All four warps of a warpgroup execute the same call; the
+// registers that .dec releases are what .inc can take, out of the block's launch allocation
+// (threads x registers per thread at launch).
+template <uint32_t N>
+__device__ __forceinline__ void regs_release_to() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_grow_to() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
