@@ -198,6 +198,23 @@ def run_reference(args, world, rank):
 
 # ------------------------------------------------------------------ GPU arm
 
+def summarize(ms):
+    """Median, p95 and the 95% Student-t interval of the mean of per-step event times (ms)."""
+    ms = np.asarray(ms, dtype=np.float64)
+    n = len(ms)
+    out = {"median": float(np.median(ms)), "p95": float(np.percentile(ms, 95)),
+           "mean": float(ms.mean()), "n": n}
+    if n > 1:
+        try:
+            from scipy.stats import t as student_t
+            q = float(student_t.ppf(0.975, n - 1))
+        except Exception:  # scipy missing: normal quantile, slightly narrow for small n
+            q = 1.96
+        half = q * float(ms.std(ddof=1)) / np.sqrt(n)
+        out["ci95"] = [out["mean"] - half, out["mean"] + half]
+    return out
+
+
 def run_ours(args, world, rank, local):
     from exact_io_aware_28_gb300 import fa
 
@@ -276,6 +293,9 @@ def run_ours(args, world, rank, local):
     phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
                       for i in range(args.steps)])  # ms: fwd, preprocess, main, convert
     step_ms = phase.sum(axis=1)
+    timing = {name: summarize(col) for name, col in
+              (("step_ms", step_ms), ("fwd_ms", phase[:, 0]), ("preprocess_ms", phase[:, 1]),
+               ("bwd_main_ms", phase[:, 2]), ("dq_convert_ms", phase[:, 3]))}
     ms_per_step = float(step_ms.mean()) if flush else t_start.elapsed_time(t_end) / args.steps
     ms_per_step = max_over_ranks(ms_per_step, world)
     value = world * fl["fwd_bwd"] / (ms_per_step * 1e-3) / 1e12
@@ -342,6 +362,8 @@ def run_ours(args, world, rank, local):
                        else f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q, K, V, dO)",
                        "flops_per_step": fl["fwd_bwd"]},
             "pct_of_peak": value / world / peak_t,
+            "pct_of_peak_burst": value / world / pk["bf16_tflops"],
+            "timing": timing,
             "phases": {"fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "bwd_main_tflops": main_tf,
                        "fwd_ms": mean_phase[0], "preprocess_ms": mean_phase[1],
                        "bwd_main_ms": mean_phase[2], "dq_convert_ms": mean_phase[3],
