@@ -211,7 +211,7 @@ def summarize(ms):
         except Exception:  # scipy missing: normal quantile, slightly narrow for small n
             q = 1.96
         half = q * float(ms.std(ddof=1)) / np.sqrt(n)
-        out["ci95"] = [out["mean"] - half, out["mean"] + half]
+        out["ci95"] = [float(out["mean"] - half), float(out["mean"] + half)]
     return out
 
 
