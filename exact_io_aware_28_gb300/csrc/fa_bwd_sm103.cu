@@ -52,8 +52,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kProducerWarp = 12;  // also allocates tensor memory
 constexpr int kMmaWarp = 13;       // warps 14-15 idle
 constexpr int kThreads = 512;
-constexpr int kRegsDrain = 200;    // warps 0-3 after reallocation (d = 128)
-constexpr int kRegsControl = 56;   // warps 12-15 after reallocation (d = 128)
+// Registers per thread after reallocation (d = 128; launched with 128).
+constexpr int kRegsDrain = 168;    // warps 0-3
+constexpr int kRegsSoftmax = 144;  // warps 4-11
+constexpr int kRegsControl = 56;   // warps 12-15
 
 template <int D>
 struct Cfg {
@@ -181,10 +183,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   const uint32_t tb = bars->tmem_base;
   const int first = next_q(p, u, -1);
   // Registers (d = 128): launched with 128 per thread (512 threads).  The producer / MMA
-  // warpgroup (warps 12-15) gives 72 of them back and the dQ drain warpgroup (warps 0-3)
-  // takes them, so a drain warp can hold a whole 128-column dQ row slice in registers:
-  // 4 x 32 x (200 + 128 + 128 + 56) = 512 x 128.  With d = 64 a slice fits as launched.
-  static_assert(kThreads == 512 && kRegsDrain + 2 * 128 + kRegsControl == 4 * 128, "register split");
+  // warpgroup (warps 12-15) gives 72 of them back; the dQ drain warpgroup (warps 0-3) takes
+  // 40, so a drain warp can hold a whole 128-column dQ row slice, and each softmax
+  // warpgroup 16, so phase A can load all 64 of its S^T columns at once:
+  // 4 x 32 x (168 + 144 + 144 + 56) = 512 x 128.  With d = 64 everything fits as launched.
+  static_assert(kThreads == 512 && kRegsDrain + 2 * kRegsSoftmax + kRegsControl == 4 * 128, "register split");
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -314,6 +317,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P^T and dS^T (key rows)
+    if constexpr (D == 128) regs_grow_to<kRegsSoftmax>();
     const int w = (warp - 4) >> 2;              // query columns [64w, 64w + 64)
     const int r = ((warp & 3) << 5) + lane;     // key row within the block = TMEM lane
     const int key = u.j * kBlk + r;
@@ -362,10 +366,12 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       const uint64_t c2 = f2_pack(c, c);
       // Off the diagonal, every query column of a live key row is visible: no masks.
       const bool masked = diag || !key_live;
+      // Both halves of this warpgroup's S^T columns in one round trip.
+      uint32_t sva[64];
+      tmem_ld64_wait(lane_base + 64 * w, lane_base + 64 * w + 32, sva);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t sv[32];
-        tmem_ld32_wait(lane_base + 64 * w + 32 * h, sv);
+        uint32_t* sv = sva + 32 * h;
         const float* L = sL + 64 * w + 32 * h;
         const float2* L2 = reinterpret_cast<const float2*>(L);
         if (!masked) {
