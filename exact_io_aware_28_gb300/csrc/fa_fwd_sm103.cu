@@ -59,6 +59,7 @@ struct Bars {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
+  uint64_t o_staged[2];  // a tile of O is in shared memory, ready for the TMA store
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -98,7 +99,7 @@ __device__ __forceinline__ int next_any(const Problem& p, const Unit& u, int j, 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                 const __grid_constant__ CUtensorMap mv, __nv_bfloat16* __restrict__ o,
+                 const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
                  float* __restrict__ lse, Problem p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -139,6 +140,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 2 * kBlk);
       mbar_init(&bars->o_done[t], 1);
+      mbar_init(&bars->o_staged[t], 2 * kBlk);
     }
     mbar_init(&bars->drain, 2);
     bars->abort = 0;
@@ -393,8 +395,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       lB += __shfl_xor_sync(0xffffffffu, lB, 2);
       const float invA = lA > 0.f ? 1.f / lA : 0.f, invB = lB > 0.f ? 1.f / lB : 0.f;
       const int rowA = u.q0 + t * kBlk + rA, rowB = rowA + 8;
-      __nv_bfloat16* oA = o + (static_cast<size_t>(u.bh) * p.N + rowA) * D;
-      __nv_bfloat16* oB = oA + 8 * D;
+      // O / l as bf16 into this tile's Q buffer (every S MMA that read it has completed: they
+      // precede the last P V product of this tile), in the 128-byte-swizzled layout of the
+      // TMA box; one thread then stores the tile with the TMA (rows past N are clipped).
+      uint8_t* stage = sQ + t * C::TILE;
 #pragma unroll
       for (int half = 0; half < D / 64; ++half) {
         uint32_t ov[32];
@@ -404,15 +408,24 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = 0u;
         }
+        uint8_t* sub = stage + half * kSub;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-          const int col = 64 * half + 8 * cc + 2 * t4;
-          if (rowA < p.N)
-            *reinterpret_cast<uint32_t*>(oA + col) =
-                pack_bf16x2(__uint_as_float(ov[4 * cc]) * invA, __uint_as_float(ov[4 * cc + 1]) * invA);
-          if (rowB < p.N)
-            *reinterpret_cast<uint32_t*>(oB + col) =
-                pack_bf16x2(__uint_as_float(ov[4 * cc + 2]) * invB, __uint_as_float(ov[4 * cc + 3]) * invB);
+          const uint32_t byte = static_cast<uint32_t>(4 * t4);   // column 8cc + 2t4, bf16
+          *reinterpret_cast<uint32_t*>(sub + rA * 128 + ((cc ^ (rA & 7)) << 4) + byte) =
+              pack_bf16x2(__uint_as_float(ov[4 * cc]) * invA, __uint_as_float(ov[4 * cc + 1]) * invA);
+          *reinterpret_cast<uint32_t*>(sub + rB * 128 + ((cc ^ (rB & 7)) << 4) + byte) =
+              pack_bf16x2(__uint_as_float(ov[4 * cc + 2]) * invB, __uint_as_float(ov[4 * cc + 3]) * invB);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->o_staged[t]);
+      if (warp == 4 && lane == 0 && u.q0 + t * kBlk < p.N) {
+        if (mbar_wait(&bars->o_staged[t], 0, abort_flag, p.err, p.wait_ns)) {
+#pragma unroll
+          for (int half = 0; half < D / 64; ++half)
+            tma_store_3d(&mo, stage + half * kSub, 64 * half, u.q0 + t * kBlk, u.bh);
+          bulk_commit_group();
         }
       }
       if (t4 == 0) {
@@ -423,6 +436,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     }
   }
 
+  if (warp == 4 && lane == 0) bulk_wait_group_all();
   tc_fence_before();
   __syncthreads();
   if (bars->abort && tid == 0) {
@@ -487,10 +501,10 @@ bool make_acc_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
 template <int D>
 static cudaError_t fwd_launch(const Problem& p, const void* q, const void* k, const void* v,
                               void* o, float* lse, cudaStream_t s) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const int BH = p.B * p.H;
   if (!make_head_map(&mq, q, BH, p.N, D) || !make_head_map(&mk, k, BH, p.N, D) ||
-      !make_head_map(&mv, v, BH, p.N, D))
+      !make_head_map(&mv, v, BH, p.N, D) || !make_head_map(&mo, o, BH, p.N, D))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -503,8 +517,7 @@ static cudaError_t fwd_launch(const Problem& p, const void* q, const void* k, co
   }
   const int nqb = (p.N + 255) / 256;
   dim3 grid(static_cast<unsigned>(BH) * nqb);
-  fwd_sm103_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, s>>>(mq, mk, mv,
-                                                            static_cast<__nv_bfloat16*>(o), lse, p);
+  fwd_sm103_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, s>>>(mq, mk, mv, mo, lse, p);
   return cudaGetLastError();
 }
 
