@@ -88,3 +88,17 @@ def bwd_min_bytes(B: int, H: int, N: int, d: int, elem: int = 2) -> int:
     """Q, K, V, O, dO, lse read once; dQ, dK, dV written once."""
     rows = B * H * N
     return rows * d * elem * 8 + rows * 4
+
+
+def decode_flops(Hq: int, d: int, cache_len) -> float:
+    """Decode FLOPs: per query head and visible key, a length-d dot product for the score
+    and a length-d multiply-add into the output (2*d + 2*d)."""
+    return 4.0 * d * Hq * float(np.asarray(cache_len, dtype=np.float64).sum())
+
+
+def decode_bytes(Hq: int, Hkv: int, d: int, cache_len, elem: int = 2) -> float:
+    """Algorithmic bytes of one decode step: the visible K and V rows read once, q read,
+    o (elem bytes) and lse (4 bytes) written."""
+    L = float(np.asarray(cache_len, dtype=np.float64).sum())
+    B = len(np.asarray(cache_len))
+    return 2.0 * L * Hkv * d * elem + B * Hq * (d * elem + d * elem + 4)

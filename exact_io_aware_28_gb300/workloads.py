@@ -119,3 +119,65 @@ def make_inputs(w: Workload, seed: int = 0, device: str = "cpu") -> Inputs:
         if blockmask is not None:
             blockmask = blockmask.to(device)
     return Inputs(q, k, v, do, kv_len, blockmask, w.causal, w.scale)
+
+
+# ------------------------------------------------------------------ decode
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One new query token per sequence over a key/value cache of up to ``L`` rows.
+
+    ``Hq`` query heads share ``Hkv`` key/value heads in contiguous groups of Hq / Hkv.
+    ``ragged``: per-sequence cache lengths drawn in [max(1, L / 2), L]; otherwise all L.
+    """
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    L: int
+    d: int
+    ragged: bool = False
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / (self.d ** 0.5)
+
+    def describe(self) -> str:
+        return (f"{self.name}: B={self.B} Hq={self.Hq} Hkv={self.Hkv} L={self.L} d={self.d} bf16"
+                + (" ragged cache lengths" if self.ragged else ""))
+
+
+# The decode shape the course page uses as its example: Llama-3-8B (32 query heads, 8
+# key/value heads, head size 128) at an 8k context, 64 sequences decoding together.
+DECODE_WORKLOADS = {
+    "decode_llama8b": DecodeWorkload("decode_llama8b", 64, 32, 8, 8192, 128),
+}
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    q: torch.Tensor          # [B, Hq, d] bf16
+    k: torch.Tensor          # [B, Hkv, L, d] bf16
+    v: torch.Tensor          # [B, Hkv, L, d] bf16
+    cache_len: torch.Tensor  # int32 [B]
+    scale: float
+
+
+def make_decode_inputs(w: DecodeWorkload, seed: int = 0, device: str = "cpu") -> DecodeInputs:
+    """Draw q, k, v (``randn`` in fp32 from one CPU generator, in that order, rounded to
+    bf16), then the cache lengths."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q = torch.randn((w.B, w.Hq, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.Hkv, w.L, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.Hkv, w.L, w.d), generator=g, dtype=torch.float32)
+    if w.ragged:
+        lo = max(1, w.L // 2)
+        cache_len = torch.randint(lo, w.L + 1, (w.B,), generator=g, dtype=torch.int64)
+    else:
+        cache_len = torch.full((w.B,), w.L, dtype=torch.int64)
+    cache_len = cache_len.to(torch.int32)
+    q, k, v = (t.to(torch.bfloat16).contiguous() for t in (q, k, v))
+    if device != "cpu":
+        q, k, v, cache_len = (t.to(device) for t in (q, k, v, cache_len))
+    return DecodeInputs(q, k, v, cache_len, w.scale)
