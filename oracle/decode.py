@@ -48,9 +48,14 @@ def decode(q, k, v, scale: float, cache_len=None, pairs=None):
     lse = np.full((B, Hq), np.nan)
     todo = pairs if pairs is not None else [(b, h) for b in range(B) for h in range(Hq)]
     for b, h in todo:
-        L = Lmax if cache_len is None else int(cache_len[b])
-        keep = (np.arange(Lmax) < L)[None, :]
+        L = Lmax if cache_len is None else max(0, min(int(cache_len[b]), Lmax))
         g = h // G
-        ob, lb, _ = forward_head(q[b, h][None, :], k[b, g], v[b, g], scale, keep)
+        # Only the first L rows of the cache belong to the sequence: attend over those
+        # alone, so nothing the rest of the buffer holds (even NaN) reaches the result.
+        if L == 0:  # no visible key: O = 0 and lse = -inf, as for a fully masked row
+            o[b, h], lse[b, h] = 0.0, -np.inf
+            continue
+        keep = np.ones((1, L), dtype=bool)
+        ob, lb, _ = forward_head(q[b, h][None, :], k[b, g, :L], v[b, g, :L], scale, keep)
         o[b, h], lse[b, h] = ob[0], lb[0]
     return o, lse

@@ -76,3 +76,16 @@ def test_lse_matches_scipy_logsumexp():
         for h in range(Hq):
             s = 0.25 * k[b, h // 2, :cache_len[b]] @ q[b, h]
             assert abs(lse[b, h] - special.logsumexp(s)) < 1e-12
+
+
+def test_rows_past_the_cache_length_do_not_matter():
+    B, Hq, Hkv, L, d = 1, 2, 1, 6, 3
+    q, k, v = _rand(B, Hq, d), _rand(B, Hkv, L, d), _rand(B, Hkv, L, d)
+    o, lse = oracle.decode(q, k, v, 0.5, np.array([4]))
+    k[:, :, 4:] = np.nan
+    v[:, :, 4:] = np.inf
+    o2, lse2 = oracle.decode(q, k, v, 0.5, np.array([4]))
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    o0, lse0 = oracle.decode(q, k, v, 0.5, np.array([0]))
+    assert np.all(o0 == 0) and np.all(np.isneginf(lse0))
