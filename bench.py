@@ -383,13 +383,171 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line, default=float), flush=True)
 
 
+# ------------------------------------------------------------------ decode (second workload)
+
+DECODE_METRIC = "decode attention: KV-cache GB/s on 1 GB300 and % of measured HBM bandwidth"
+
+
+def decode_oracle_seconds(w, x, pairs=None):
+    import oracle  # test infrastructure: the CPU baseline leg only
+    t0 = time.perf_counter()
+    oracle.decode(x.q.double().numpy(), x.k.double().numpy(), x.v.double().numpy(), w.scale,
+                  x.cache_len.numpy(), pairs)
+    return time.perf_counter() - t0
+
+
+def decode_cpu_baseline(w, x_cpu) -> dict:
+    # A bounded sample: the query heads of the first 8 sequences (the fp64 conversion of the
+    # whole cache alone would take most of the budget), scaled to the metric's bytes.
+    nb = min(8, w.B)
+    sub = W.DecodeInputs(x_cpu.q[:nb], x_cpu.k[:nb], x_cpu.v[:nb], x_cpu.cache_len[:nb], w.scale)
+    secs = decode_oracle_seconds(w, sub)
+    gb = acc.decode_bytes(w.Hq, w.Hkv, w.d, sub.cache_len.numpy()) / 1e9
+    return {"value": gb / secs, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{nb} of {w.B} sequences of {w.describe()}: fp64 NumPy, {secs:.2f} s"}
+
+
+def run_decode_reference(args, world, rank):
+    """The CPU fp64 oracle on the decode workload, a bounded sample per step."""
+    if rank != 0:
+        return
+    w = W.DECODE_WORKLOADS[args.workload]
+    x = W.make_decode_inputs(w, seed=0)
+    nb = min(4, w.B)
+    sub = W.DecodeInputs(x.q[:nb], x.k[:nb], x.v[:nb], x.cache_len[:nb], w.scale)
+    timed = max(1, min(args.steps, 20))
+    times = [decode_oracle_seconds(w, sub) for _ in range(timed)]
+    mean = sum(times) / len(times)
+    value = acc.decode_bytes(w.Hq, w.Hkv, w.d, sub.cache_len.numpy()) / 1e9 / mean
+    sample = f"{nb} of {w.B} sequences per step, {timed} of {args.steps} steps timed"
+    print(json.dumps({
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.describe(), "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_decode(args, world, rank, local):
+    """Decode over a KV cache: fa_decode per step, KV bytes read / event time."""
+    from exact_io_aware_28_gb300 import fa
+    w = W.DECODE_WORKLOADS[args.workload]
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: the product path has no CPU fallback")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load()
+    x_cpu = W.make_decode_inputs(w, seed=0)
+    x = W.DecodeInputs(*(t.to(dev) for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.cache_len)),
+                       w.scale)
+    stream = torch.cuda.current_stream(dev)
+    o = torch.empty_like(x.q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.L, w.d), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        fa.fa_decode(x.q, x.k, x.v, o, lse, ws, x.cache_len, x.scale, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_error() != fa.FA_OK:
+        raise RuntimeError("device error word set during warm-up")
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for e0, e1 in evs:
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    if fa.fa_device_error() != fa.FA_OK:
+        raise RuntimeError("device error word set during the timed region")
+    ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
+    ms_per_step = max_over_ranks(float(ms.mean()), world)
+    cl = x_cpu.cache_len.numpy()
+    nbytes = acc.decode_bytes(w.Hq, w.Hkv, w.d, cl)
+    gbs = world * nbytes / (ms_per_step * 1e-3) / 1e9
+    pk = peaks()
+    tflops = world * acc.decode_flops(w.Hq, w.d, cl) / (ms_per_step * 1e-3) / 1e12
+
+    # e2e: the cache, the queries and the lengths come from pinned host memory every step and
+    # o, lse go back.
+    pin = [t.pin_memory() for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.cache_len)]
+    outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+    e2e_steps = max(1, min(args.steps, 3))
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        for hsrc, ddst in zip(pin, (x.q, x.k, x.v, x.cache_len)):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        for hdst, dsrc in zip(outs, (o, lse)):
+            hdst.copy_(dsrc, non_blocking=True)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = decode_cpu_baseline(w, x_cpu)
+    if rank == 0:
+        splits = None
+        try:
+            splits = fa.fa_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.L, w.d) // (
+                w.B * w.Hq * (w.d + 4) * 4)
+        except Exception:
+            pass
+        print(json.dumps({
+            "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.describe(), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "L": w.L,
+                       "d": w.d, "splits": splits,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB of KV cache)",
+                       "bytes_per_step": nbytes},
+            "tflops": tflops,
+            "timing": {"step_ms": summarize(ms)},
+            "roofline": {"kernel": "decode split kernel + combine", "bound": "hbm",
+                         "achieved": gbs / world, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / world / pk["hbm_gbs"], "traffic": None,
+                         "peak_kind": f"{pk['source']} HBM copy bandwidth"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "steps": e2e_steps},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+        }, default=float), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=W.ORDER, default="long_causal")
+    ap.add_argument("--workload", choices=W.ORDER + list(W.DECODE_WORKLOADS),
+                    default="long_causal")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the workload's head count (smaller cases for profiling)")
@@ -397,10 +555,11 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     world, rank, local = dist_setup()
+    decode = args.workload in W.DECODE_WORKLOADS
     if args.impl == "reference":
-        run_reference(args, world, rank)
+        (run_decode_reference if decode else run_reference)(args, world, rank)
     else:
-        run_ours(args, world, rank, local)
+        (run_decode if decode else run_ours)(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

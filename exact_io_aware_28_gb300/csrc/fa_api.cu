@@ -73,6 +73,37 @@ using namespace fa;
 
 extern "C" {
 
+size_t fa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return 0;
+  if (d != 64 && d != 128) return 0;
+  const size_t splits = static_cast<size_t>(decode_splits(B, Hkv, Lmax));
+  return static_cast<size_t>(B) * Hq * splits * (d + 4) * sizeof(float);
+}
+
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int Hq, int Hkv, int Lmax, int d, const int32_t* cache_len,
+                    float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * Hkv > 65535 || Lmax > (1 << 24)) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace))
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cache_len) & 3u) != 0) return FA_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fa_decode_workspace_bytes(B, Hq, Hkv, Lmax, d)) return FA_ERR_INVALID_ARG;
+  int* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  const int splits = decode_splits(B, Hkv, Lmax);
+  cudaError_t e = launch_decode(q, k, v, o, lse, B, Hq, Hkv, Lmax, d, cache_len, scale,
+                                static_cast<float*>(workspace), splits, err, wait_limit_ns(),
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "FA_OK";

@@ -467,19 +467,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// [B*H, N, d] bf16 viewed as a 3-D tensor (d innermost); 64 x 128 boxes, 128B swizzle,
-// rows beyond N read as zero.
-bool make_head_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+// [B*H, N, d] bf16 viewed as a 3-D tensor (d innermost); 64-column boxes of `box_rows` rows,
+// 128B swizzle, rows beyond N read as zero.
+bool make_head_map_rows(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_head_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+  return make_head_map_rows(map, ptr, BH, N, d, 128);
 }
 
 // [B*H, N, d] fp32 accumulator as a 3-D tensor with 32 x 32 boxes (128-byte rows, 128-byte

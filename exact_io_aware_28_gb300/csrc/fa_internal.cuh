@@ -48,6 +48,16 @@ cudaError_t launch_bwd_sm103(const Problem& p, const void* q, const void* k, con
 // Tensor map of a [B*H, N, d] bf16 tensor (d innermost) with 64 x 128 boxes and 128-byte
 // swizzle; rows beyond N read as zero.  Returns false if the driver rejects it.
 bool make_head_map(CUtensorMap* map, const void* ptr, int BH, int N, int d);
+// The same view with 64-column boxes of `box_rows` rows (1..256).
+bool make_head_map_rows(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows);
+
+// Decode over a key/value cache (split kernel + combine kernel); see fa_decode.cu.
+cudaError_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int Lmax, int d, const int32_t* cache_len,
+                          float scale, float* partials, int splits, int* err,
+                          unsigned long long wait_ns, cudaStream_t s);
+// Number of key splits per (sequence, key/value head) the decode uses on this device.
+int decode_splits(int B, int Hkv, int Lmax);
 
 // Tensor map of a [B*H, N, d] fp32 accumulator with 32 x 32 boxes (128-byte swizzle), for bulk
 // reduce-add; rows beyond N are outside the map.

@@ -21,7 +21,7 @@ FA_BF16, FA_FP32 = 0, 1
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_preprocess", "fa_bwd_main",
            "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_status_string", "fa_device_error",
-           "fa_selftest_wait_timeout")
+           "fa_selftest_wait_timeout", "fa_decode_workspace_bytes", "fa_decode")
 
 # Largest workspace (bytes) fa_bwd_noalloc can serve from its built-in scratch array.
 FA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -66,6 +66,10 @@ def load() -> ctypes.CDLL:
     lib.fa_device_error.restype = I
     lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, P]
     lib.fa_selftest_wait_timeout.restype = I
+    lib.fa_decode_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.fa_decode_workspace_bytes.restype = S
+    lib.fa_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, P, F, P, S, P]
+    lib.fa_decode.restype = I
     _lib = lib
     return lib
 
@@ -223,3 +227,40 @@ def backward(q, k, v, o, lse, do, causal=False, blockmask=None, kv_len=None, sca
         workspace = alloc_workspace(B, H, N, d, q.device)
     fa_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, causal, blockmask, kv_len, scale, stream)
     return dq, dk, dv
+
+
+# ----------------------------------------------------------- decode
+
+def fa_decode_workspace_bytes(B: int, Hq: int, Hkv: int, Lmax: int, d: int) -> int:
+    return int(load().fa_decode_workspace_bytes(B, Hq, Hkv, Lmax, d))
+
+
+def fa_decode(q, k, v, o, lse, workspace, cache_len=None, scale=None, stream=None):
+    """q [B, Hq, d], k/v [B, Hkv, Lmax, d] bf16; o [B, Hq, d] bf16, lse [B, Hq] fp32 out."""
+    _check_dense(q, k, v, o, lse, cache_len, workspace)
+    B, Hq, d = q.shape
+    Hkv, Lmax = k.shape[1], k.shape[2]
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("decode takes bf16 q, k, v")
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    st = load().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Lmax, d,
+                          _ptr(cache_len), float(scale), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_decode")
+
+
+def decode(q, k, v, cache_len=None, scale=None, workspace=None, stream=None):
+    """Allocate o, lse (and the workspace unless given) with torch and run fa_decode."""
+    B, Hq, d = q.shape
+    Hkv, Lmax = k.shape[1], k.shape[2]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = fa_decode_workspace_bytes(B, Hq, Hkv, Lmax, d)
+        if n == 0:
+            raise FaError(FA_ERR_INVALID_ARG, "fa_decode_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    fa_decode(q, k, v, o, lse, workspace, cache_len, scale, stream)
+    return o, lse

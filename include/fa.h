@@ -156,6 +156,32 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          const uint8_t* blockmask, const int32_t* kv_len,
                          float scale, fa_dtype dtype, void* stream);
 
+/*
+ * Decode attention over a key/value cache with grouped key/value heads: one new query token
+ * per sequence (course page week 13, step 1, the bullet on attention in decode: every
+ * sequence has its own cache, the step reads it once at about Hq / Hkv FLOP per byte).
+ *   q         in : bf16 [B, Hq, d], the new tokens' queries.
+ *   k, v      in : bf16 [B, Hkv, Lmax, d], the caches; query head h reads key/value head
+ *                  h / (Hq / Hkv) (contiguous groups).
+ *   cache_len in : NULL (every sequence has Lmax keys) or device int32 [B]; keys
+ *                  j >= cache_len[b] are ignored and never read into the result, whatever
+ *                  those rows hold.  Values are clamped to [0, Lmax] on the device.
+ *   o         out: bf16 [B, Hq, d] = softmax(scale q K^T) V over the visible keys; 0 for a
+ *                  sequence with no key.
+ *   lse       out: fp32 [B, Hq], natural-log logsumexp of the scaled scores (-inf: no key).
+ *   scale        : multiplier of q K^T, normally 1/sqrt(d); finite and > 0.
+ *   workspace    : device buffer of at least fa_decode_workspace_bytes(B, Hq, Hkv, Lmax, d)
+ *                  bytes, 16-byte aligned, for the per-split fp32 partial results; its
+ *                  contents on entry do not matter.
+ * Supported: d in {64, 128}; Hq / Hkv in {1, 2, 4, 8} (FA_ERR_UNSUPPORTED otherwise);
+ * Hq must be a multiple of Hkv (FA_ERR_INVALID_ARG otherwise).  Two kernels run on
+ * `stream`: the split kernel and the combine kernel.
+ */
+size_t fa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int d);
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int Hq, int Hkv, int Lmax, int d, const int32_t* cache_len,
+                    float scale, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 

@@ -112,3 +112,41 @@ def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fa, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         fa.load()
+
+
+def dec(**kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=2, Hq=8, Hkv=2, L=300, d=128, cl=None,
+                scale=0.088, ws=A, wsb=1 << 30)
+    args.update(kw)
+    lib = fa.load()
+    return lib.fa_decode(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                         args["Hq"], args["Hkv"], args["L"], args["d"], args["cl"],
+                         args["scale"], args["ws"], args["wsb"], None)
+
+
+def test_decode_workspace_bytes():
+    n = fa.fa_decode_workspace_bytes(2, 8, 2, 300, 128)
+    per_split = 2 * 8 * (128 + 4) * 4
+    assert n > 0 and n % per_split == 0
+    assert fa.fa_decode_workspace_bytes(2, 8, 3, 300, 128) == 0   # 8 % 3 != 0
+    assert fa.fa_decode_workspace_bytes(2, 8, 2, 300, 96) == 0
+    assert fa.fa_decode_workspace_bytes(0, 8, 2, 300, 128) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"q": None}, fa.FA_ERR_INVALID_ARG),
+    ({"ws": None}, fa.FA_ERR_INVALID_ARG),
+    ({"wsb": 16}, fa.FA_ERR_INVALID_ARG),
+    ({"Hkv": 3}, fa.FA_ERR_INVALID_ARG),          # query heads not a multiple of K/V heads
+    ({"Hq": 12, "Hkv": 4}, fa.FA_ERR_UNSUPPORTED),  # three query heads per K/V head
+    ({"Hq": 32, "Hkv": 2}, fa.FA_ERR_UNSUPPORTED),  # sixteen
+    ({"d": 96}, fa.FA_ERR_UNSUPPORTED),
+    ({"L": 0}, fa.FA_ERR_INVALID_ARG),
+    ({"k": A + 8}, fa.FA_ERR_INVALID_ARG),
+    ({"lse": A + 2}, fa.FA_ERR_INVALID_ARG),
+    ({"cl": A + 1}, fa.FA_ERR_INVALID_ARG),
+    ({"scale": 0.0}, fa.FA_ERR_INVALID_ARG),
+    ({"scale": float("nan")}, fa.FA_ERR_INVALID_ARG),
+])
+def test_decode_rejects_bad_arguments(kw, code):
+    assert dec(**kw) == code
