@@ -435,6 +435,8 @@ def run_decode(args, world, rank, local):
     """Decode over a KV cache: fa_decode per step, KV bytes read / event time."""
     from exact_io_aware_28_gb300 import fa
     w = W.DECODE_WORKLOADS[args.workload]
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch)
     if not torch.cuda.is_available():
         raise RuntimeError("no CUDA device: the product path has no CPU fallback")
     dev = torch.device("cuda", local)
@@ -551,6 +553,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the workload's head count (smaller cases for profiling)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="decode workloads: override the number of sequences (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -13,8 +13,9 @@
 // threads, two CTAs per SM.  Thread 0 streams 64-key tiles of K and V into a three-stage
 // ring with TMA (128-byte swizzle, mbarrier completion, bounded waits; a result that differs
 // between threads is settled with a CTA-wide AND before anyone leaves the loop).  Per tile:
-//   scores  -- thread (key j, quarter of d) forms partial dot products with the G queries
-//              (fp32, scale * log2(e) folded into q); the four quarters are summed by
+//   scores  -- each thread keeps a slice of d of the G queries in registers (fp32, scale *
+//              log2(e) folded in) and forms partial dot products for a few keys; the
+//              slices of a key are neighbouring lanes, summed by shuffles; then
 //   softmax -- one warp per query head: tile maximum and sum by shuffles, running maximum
 //              m and sum l, probabilities and the rescale factor into shared memory;
 //   P V     -- thread (pair of output columns, group of keys) accumulates all G heads.
@@ -45,12 +46,21 @@ struct DCfg {
   static constexpr int NSUB = D / 64;
   static constexpr int TILE = NSUB * kSubBytes;   // bytes of a K (or V) tile
   static constexpr int STAGE = 2 * TILE;          // K tile then V tile
-  static constexpr int PARTS = 4;                 // quarters of d in the score phase
-  static constexpr int DPART = D / PARTS;         // 32 or 16 columns
   static constexpr int NDP = D / 2;               // column pairs of the P V phase
   static constexpr int KGROUPS = kThreads / NDP;  // key groups of the P V phase: 4 or 8
   static constexpr int KPER = kTile / KGROUPS;    // keys per P V thread: 16 or 8
   static constexpr int PSTRIDE = D + 4;           // floats per (split, head) partial row
+};
+
+// Score-phase split of d: each thread keeps its slice of the G queries in registers (at most
+// 64 floats) and serves KPT keys; the NPART slices of a key are neighbouring lanes.
+template <int D, int G>
+struct SCfg {
+  static constexpr int NPART = (D * G / 64) > 4 ? (D * G / 64) : 4;
+  static constexpr int DPART = D / NPART;   // 64 .. 8 columns
+  static constexpr int KPW = 32 / NPART;    // keys per warp pass
+  static constexpr int KPT = NPART / 4;     // keys per thread per 64-key tile
+  static_assert(DPART % 8 == 0 && KPW * KPT * 8 == kTile, "score split");
 };
 
 struct DBars {
@@ -72,8 +82,7 @@ __device__ __forceinline__ float2 bf2f(uint32_t w) {
 template <int D, int G>
 constexpr int decode_smem_bytes() {
   using C = DCfg<D>;
-  return 1024 + kStages * C::STAGE +
-         4 * (G * D + C::PARTS * kTile * G + kTile * G + 8) + static_cast<int>(sizeof(DBars));
+  return 1024 + kStages * C::STAGE + 4 * (2 * kTile * G + 8) + static_cast<int>(sizeof(DBars));
 }
 
 template <int D, int G>
@@ -86,9 +95,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-  float* qs = reinterpret_cast<float*>(stages + kStages * C::STAGE);  // [G][D]
-  float* sp = qs + G * D;                                             // [PARTS][kTile][G]
-  float* pb = sp + C::PARTS * kTile * G;                              // [kTile][G]
+  float* sp = reinterpret_cast<float*>(stages + kStages * C::STAGE);  // [kTile][G] scores
+  float* pb = sp + kTile * G;                                         // [kTile][G]
   float* alpha_s = pb + kTile * G;                                    // [G] (8 slots)
   DBars* bars = reinterpret_cast<DBars*>(alpha_s + 8);
 
@@ -104,9 +112,26 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
   const int k1 = min(k0 + chunk, L);
   const int ntiles = k1 > k0 ? (k1 - k0 + kTile - 1) / kTile : 0;
 
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int h = i / D, col = i % D;
-    qs[i] = __bfloat162float(q[(static_cast<size_t>(b) * Hq + g * G + h) * D + col]) * c;
+  // This thread's slice of the G queries, scaled by scale * log2(e), kept in registers.
+  using S = SCfg<D, G>;
+  const int spart = lane % S::NPART;
+  float qr[G][S::DPART];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const __nv_bfloat16* qh = q + (static_cast<size_t>(b) * Hq + g * G + h) * D + spart * S::DPART;
+#pragma unroll
+    for (int i = 0; i < S::DPART; i += 8) {
+      const uint4 w = *reinterpret_cast<const uint4*>(qh + i);
+      const float2 a = bf2f(w.x), bq = bf2f(w.y), cq = bf2f(w.z), dq = bf2f(w.w);
+      qr[h][i] = a.x * c;
+      qr[h][i + 1] = a.y * c;
+      qr[h][i + 2] = bq.x * c;
+      qr[h][i + 3] = bq.y * c;
+      qr[h][i + 4] = cq.x * c;
+      qr[h][i + 5] = cq.y * c;
+      qr[h][i + 6] = dq.x * c;
+      qr[h][i + 7] = dq.y * c;
+    }
   }
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) mbar_init(&bars->full[st], 1);
@@ -131,7 +156,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
     for (int t = 0; t < kStages && t < ntiles; ++t) issue(t);
   }
 
-  const int sj = tid & (kTile - 1), spart = tid / kTile;  // score phase: key, quarter of d
   const int dp = tid % C::NDP, kg = tid / C::NDP;         // P V phase: column pair, key group
   float o_acc[G][2];
 #pragma unroll
@@ -146,34 +170,42 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
     const uint8_t* kt = stages + st * C::STAGE;
     const uint8_t* vt = kt + C::TILE;
     const int valid = min(kTile, k1 - (k0 + t * kTile));  // keys of this tile inside the range
-    // ---- partial scores over this thread's quarter of d
-    {
+    // ---- scores: partial dot products over this thread's slice of d, summed over the
+    // NPART neighbouring lanes that hold the other slices of the same key
+#pragma unroll
+    for (int kk = 0; kk < S::KPT; ++kk) {
+      const int j = (warp * S::KPT + kk) * S::KPW + lane / S::NPART;
       float acc[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) acc[h] = 0.f;
-      const int col0 = spart * C::DPART;
 #pragma unroll
-      for (int cc = 0; cc < C::DPART; cc += 8) {
-        const uint4 w = *reinterpret_cast<const uint4*>(kt + swz(sj, col0 + cc));
+      for (int cc = 0; cc < S::DPART; cc += 8) {
+        const uint4 w = *reinterpret_cast<const uint4*>(kt + swz(j, spart * S::DPART + cc));
         const float2 k01 = bf2f(w.x), k23 = bf2f(w.y), k45 = bf2f(w.z), k67 = bf2f(w.w);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float4 qa = *reinterpret_cast<const float4*>(qs + h * D + col0 + cc);
-          const float4 qb = *reinterpret_cast<const float4*>(qs + h * D + col0 + cc + 4);
           float a = acc[h];
-          a = fmaf(qa.x, k01.x, a);
-          a = fmaf(qa.y, k01.y, a);
-          a = fmaf(qa.z, k23.x, a);
-          a = fmaf(qa.w, k23.y, a);
-          a = fmaf(qb.x, k45.x, a);
-          a = fmaf(qb.y, k45.y, a);
-          a = fmaf(qb.z, k67.x, a);
-          a = fmaf(qb.w, k67.y, a);
+          a = fmaf(qr[h][cc], k01.x, a);
+          a = fmaf(qr[h][cc + 1], k01.y, a);
+          a = fmaf(qr[h][cc + 2], k23.x, a);
+          a = fmaf(qr[h][cc + 3], k23.y, a);
+          a = fmaf(qr[h][cc + 4], k45.x, a);
+          a = fmaf(qr[h][cc + 5], k45.y, a);
+          a = fmaf(qr[h][cc + 6], k67.x, a);
+          a = fmaf(qr[h][cc + 7], k67.y, a);
           acc[h] = a;
         }
       }
 #pragma unroll
-      for (int h = 0; h < G; ++h) sp[(spart * kTile + sj) * G + h] = acc[h];
+      for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int off = S::NPART / 2; off > 0; off >>= 1)
+          acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], off);
+      }
+      if (spart == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) sp[j * G + h] = acc[h];
+      }
     }
     __syncthreads();
     // ---- online softmax: warp h handles head h (keys lane and lane + 32)
@@ -183,10 +215,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int j = lane + 32 * e;
-        float v = 0.f;
-#pragma unroll
-        for (int pq = 0; pq < C::PARTS; ++pq) v += sp[(pq * kTile + j) * G + h];
-        s2[e] = j < valid ? v : -INFINITY;
+        s2[e] = j < valid ? sp[j * G + h] : -INFINITY;
       }
       float mx = fmaxf(s2[0], s2[1]);
 #pragma unroll
@@ -218,11 +247,27 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
         const int j = kg * C::KPER + jj;
         if (j < valid) {  // rows past the range may hold anything, even NaN: never read them
           const float2 vv = bf2f(*reinterpret_cast<const uint32_t*>(vt + swz(j, 2 * dp)));
+          float pr[G];
+          if constexpr (G >= 4) {
+#pragma unroll
+            for (int h4 = 0; h4 < G; h4 += 4) {
+              const float4 p4 = *reinterpret_cast<const float4*>(pb + j * G + h4);
+              pr[h4] = p4.x;
+              pr[h4 + 1] = p4.y;
+              pr[h4 + 2] = p4.z;
+              pr[h4 + 3] = p4.w;
+            }
+          } else if constexpr (G == 2) {
+            const float2 p2 = *reinterpret_cast<const float2*>(pb + j * G);
+            pr[0] = p2.x;
+            pr[1] = p2.y;
+          } else {
+            pr[0] = pb[j];
+          }
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float pr = pb[j * G + h];
-            o_acc[h][0] = fmaf(pr, vv.x, o_acc[h][0]);
-            o_acc[h][1] = fmaf(pr, vv.y, o_acc[h][1]);
+            o_acc[h][0] = fmaf(pr[h], vv.x, o_acc[h][0]);
+            o_acc[h][1] = fmaf(pr[h], vv.y, o_acc[h][1]);
           }
         }
       }
