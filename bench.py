@@ -220,6 +220,47 @@ def summarize(ms):
     return out
 
 
+def pipelined_e2e(steps, host_in, dev_in, dev_out, host_out, compute, comp_stream):
+    """End-to-end time per step with the copies inside the timed region.
+
+    Every step copies its inputs from pinned host memory (``host_in``) to the device and its
+    results back to pinned host memory (``host_out``).  Two device buffer sets
+    (``dev_in[0|1]``, ``dev_out[0|1]``) let step i+1's inputs travel on one copy stream and
+    step i-1's results on another while step i computes, as a pipelined caller would run it.
+    ``compute(inputs, outputs)`` launches one step on ``comp_stream``.  Returns ms per step.
+    """
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(steps)]
+    done = [torch.cuda.Event() for _ in range(steps)]
+    copied = [torch.cuda.Event() for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(h2d_s)
+    for i in range(steps):
+        k = i & 1
+        with torch.cuda.stream(h2d_s):
+            if i >= 2:
+                h2d_s.wait_event(done[i - 2])  # buffer set k is free again
+            for hsrc, ddst in zip(host_in, dev_in[k]):
+                ddst.copy_(hsrc, non_blocking=True)
+            in_ready[i].record(h2d_s)
+        comp_stream.wait_event(in_ready[i])
+        if i >= 2:
+            comp_stream.wait_event(copied[i - 2])  # its results have left output set k
+        compute(dev_in[k], dev_out[k])
+        done[i].record(comp_stream)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(done[i])
+            for hdst, dsrc in zip(host_out, dev_out[k]):
+                hdst.copy_(dsrc, non_blocking=True)
+            copied[i].record(d2h_s)
+    d2h_s.wait_event(copied[steps - 1])
+    t1.record(d2h_s)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
 def run_ours(args, world, rank, local):
     from exact_io_aware_28_gb300 import fa
 
@@ -327,29 +368,31 @@ def run_ours(args, world, rank, local):
                 "frac": main_tf / peak_t, "traffic": traffic,
                 "peak_kind": f"{pk['source']} bf16 dense, sustained"}
 
-    # e2e: the same step through the public API with host buffers and copies timed.
+    # e2e: the same step through the public API with every step's inputs copied from pinned
+    # host memory and its results copied back, inside the timed region (pipelined).
     pin = [t.pin_memory() for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.do)]
     outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
-    e2e_steps = max(1, min(args.steps, 5))
-    dev_in = (x.q, x.k, x.v, x.do)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        for hsrc, ddst in zip(pin, dev_in):
-            ddst.copy_(hsrc, non_blocking=True)
-        step()
-        for hdst, dsrc in zip(outs, (o, lse, dq, dk, dv)):
-            hdst.copy_(dsrc, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    e2e_steps = max(2, min(args.steps, 6))
+    dev_in = [(x.q, x.k, x.v, x.do), tuple(torch.empty_like(t) for t in (x.q, x.k, x.v, x.do))]
+    dev_out = [(o, lse, dq, dk, dv), tuple(torch.empty_like(t) for t in (o, lse, dq, dk, dv))]
+
+    def compute(inp, out):
+        q_, k_, v_, do_ = inp
+        o_, lse_, dq_, dk_, dv_ = out
+        fa.fa_fwd(q_, k_, v_, o_, lse_, x.causal, x.blockmask, x.kv_len, x.scale, stream)
+        fa.fa_bwd_preprocess(o_, do_, ws, stream)
+        fa.fa_bwd_main(q_, k_, v_, lse_, do_, dq_, dk_, dv_, ws, x.causal, x.blockmask,
+                       x.kv_len, x.scale, stream)
+        fa.fa_bwd_dq_convert(dq_, ws, x.scale, stream)
+
+    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, compute, stream),
+                            world)
+    del dev_in, dev_out
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs)
     e2e = {"value": world * fl["fwd_bwd"] / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "steps": e2e_steps}
+           "steps": e2e_steps, "copies": "pipelined: step i+1 in and step i-1 out during step i"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -489,22 +532,20 @@ def run_decode(args, world, rank, local):
     tflops = world * acc.decode_flops(w.Hq, w.d, cl) / (ms_per_step * 1e-3) / 1e12
 
     # e2e: the cache, the queries and the lengths come from pinned host memory every step and
-    # o, lse go back.
+    # o, lse go back (pipelined as for the attention step).
     pin = [t.pin_memory() for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.cache_len)]
     outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
-    e2e_steps = max(1, min(args.steps, 3))
-    torch.cuda.synchronize()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(e2e_steps):
-        for hsrc, ddst in zip(pin, (x.q, x.k, x.v, x.cache_len)):
-            ddst.copy_(hsrc, non_blocking=True)
-        step()
-        for hdst, dsrc in zip(outs, (o, lse)):
-            hdst.copy_(dsrc, non_blocking=True)
-    a1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / e2e_steps, world)
+    e2e_steps = max(2, min(args.steps, 4))
+    dev_in = [(x.q, x.k, x.v, x.cache_len),
+              tuple(torch.empty_like(t) for t in (x.q, x.k, x.v, x.cache_len))]
+    dev_out = [(o, lse), (torch.empty_like(o), torch.empty_like(lse))]
+
+    def compute(inp, out):
+        fa.fa_decode(inp[0], inp[1], inp[2], out[0], out[1], ws, inp[3], x.scale, stream)
+
+    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, compute, stream),
+                            world)
+    del dev_in, dev_out
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs)
     cpu = None
@@ -536,7 +577,8 @@ def run_decode(args, world, rank, local):
             "cpu_baseline": cpu,
             "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "steps": e2e_steps},
+                    "steps": e2e_steps,
+                    "copies": "pipelined: step i+1 in and step i-1 out during step i"},
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
         }, default=float), flush=True)
