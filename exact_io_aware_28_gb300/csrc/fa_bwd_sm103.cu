@@ -400,6 +400,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
       // ---- phase B: dS^T = P^T o (dP^T - D)
+      // -D of the first half's columns, read while dP^T is still being computed.
+      const float4* D4 = reinterpret_cast<const float4*>(sD + 64 * w);
+      float4 dvals[8];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) dvals[e4] = D4[e4];
       ok = mbar_wait_warp(&bars->dp_full, n & 1, abort_flag, p.err, p.wait_ns);
       // Two drain warps staged the previous dQ partial in the dS^T tile.
       if (ok && n > 0) ok = mbar_wait_warp(&bars->sds_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
@@ -408,11 +413,14 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t dpv[32], dsp[16];
+        if (h == 1) {  // the second half's -D, in flight during the TMEM load
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) dvals[e4] = D4[8 + e4];
+        }
         tmem_ld32_wait(lane_base + 128 + 64 * w + 32 * h, dpv);
-        const float4* D4 = reinterpret_cast<const float4*>(sD + 64 * w + 32 * h);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 nd = D4[e4];   // -D
+          const float4 nd = dvals[e4];   // -D
           const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * h + 2 * e4]));
           const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * h + 2 * e4 + 1]));
           const float2 d01 = f2_unpack(fmul2(f2_pack(p01.x, p01.y),
