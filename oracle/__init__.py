@@ -1,4 +1,4 @@
-"""CPU fp64 oracle for exact attention (forward, logsumexp, backward, decode).
+"""CPU fp64 oracle for exact attention (forward, logsumexp, backward, decode, FP8 forward).
 
 TEST INFRASTRUCTURE ONLY: imported by the tests, by the package's ``smoke()``
 check and by the benchmark's ``cpu_baseline`` leg, never by the product path.
@@ -7,6 +7,7 @@ from .attention import (keep_mask, scores, softmax_rows, forward_head, backward_
                         row_dot, forward, backward)
 from .online_softmax import tiled_forward_head
 from .decode import decode
+from . import fp8
 
 __all__ = ["keep_mask", "scores", "softmax_rows", "forward_head", "backward_head",
-           "row_dot", "forward", "backward", "tiled_forward_head", "decode"]
+           "row_dot", "forward", "backward", "tiled_forward_head", "decode", "fp8"]
