@@ -584,13 +584,197 @@ def run_decode(args, world, rank, local):
         }, default=float), flush=True)
 
 
+# ------------------------------------------------------------------ FP8 forward
+
+FP8_METRIC = ("FP8 (e4m3) attention forward TFLOP/s on 1 GB300, bf16 inputs encoded on the "
+              "device inside the step, and % of dense fp8 tensor peak")
+
+
+def fp8_oracle_head_seconds(x, head) -> float:
+    """The oracle's encoding of one (b, h) head and its forward on the decoded inputs."""
+    from oracle import fp8 as ofp8  # test infrastructure: the CPU legs only
+    import oracle
+    b, h = head
+    sl = (slice(b, b + 1), slice(h, h + 1))
+    q, k, v = (t[sl].to(torch.float64).numpy() for t in (x.q, x.k, x.v))
+    t0 = time.perf_counter()
+    q8, sq = ofp8.quantize_blocks(q)
+    k8, sk = ofp8.quantize_blocks(k)
+    v8, sv = ofp8.quantize_heads(v)
+    Q, K = ofp8.dequantize_blocks(q8, sq)[0, 0], ofp8.dequantize_blocks(k8, sk)[0, 0]
+    V = (v8 * sv[:, :, None, None])[0, 0]
+    keep = oracle.keep_mask(Q.shape[0], x.causal)
+    oracle.forward_head(Q, K, V, x.scale, keep)
+    return time.perf_counter() - t0
+
+
+def run_fp8_reference(args, world, rank):
+    """The CPU oracle (encoding + fp64 forward) on one (b, h) head of the workload per step."""
+    if rank != 0:
+        return
+    w = W.FP8_WORKLOADS[args.workload]
+    x = W.make_inputs(w, seed=0)
+    small = W.make_inputs(W.custom("warm", 1, 1, 256, w.d, causal=w.causal), seed=1)
+    for _ in range(args.warmup):
+        fp8_oracle_head_seconds(small, (0, 0))
+    timed = max(1, min(args.steps, 20))
+    times = [fp8_oracle_head_seconds(x, (0, i % w.H)) for i in range(timed)]
+    mean = sum(times) / len(times)
+    value = acc.flops(1, 1, w.N, w.d, w.causal)["fwd"] / mean / 1e12
+    sample = f"one (batch, head) of {w.describe()} per step; {timed} of {args.steps} steps timed"
+    print(json.dumps({
+        "impl": "reference", "metric": FP8_METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.describe(), "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_fp8(args, world, rank, local):
+    """One step = encode Q, K, V to e4m3 (3 + 1 kernels) + the e4m3 forward (1 kernel)."""
+    from exact_io_aware_28_gb300 import fa
+    w = W.FP8_WORKLOADS[args.workload]
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads)
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: the product path has no CPU fallback")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load()
+    x_cpu = W.make_inputs(w, seed=0)
+    q, k, v = (t.to(dev) for t in (x_cpu.q, x_cpu.k, x_cpu.v))
+    B, H, N, d = w.B, w.H, w.N, w.d
+    nb = (N + 127) // 128
+    Np = nb * 128
+    stream = torch.cuda.current_stream(dev)
+
+    def buffers():
+        return (torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
+                torch.empty((B, H, nb), dtype=torch.float32, device=dev),
+                torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
+                torch.empty((B, H, nb), dtype=torch.float32, device=dev),
+                torch.empty((B, H, d, Np), dtype=torch.uint8, device=dev),
+                torch.empty((B, H), dtype=torch.float32, device=dev))
+
+    enc = buffers()
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+
+    def run(inp, out, e, ev=None):
+        q8, sq, k8, sk, vt8, sv = e
+        if ev:
+            ev[0].record(stream)
+        fa.fa_fp8_quantize_qk(inp[0], q8, sq, stream)
+        fa.fa_fp8_quantize_qk(inp[1], k8, sk, stream)
+        fa.fa_fp8_quantize_v(inp[2], vt8, sv, stream)
+        if ev:
+            ev[1].record(stream)
+        fa.fa_fwd_fp8(q8, k8, vt8, sq, sk, sv, out[0], out[1], w.causal, None, None, w.scale,
+                      stream)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        run((q, k, v), (o, lse), enc)
+    torch.cuda.synchronize()
+    if fa.fa_device_error() != fa.FA_OK:
+        raise RuntimeError("device error word set during warm-up")
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        run((q, k, v), (o, lse), enc, evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    if fa.fa_device_error() != fa.FA_OK:
+        raise RuntimeError("device error word set during the timed region")
+    phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(2)]
+                      for i in range(args.steps)])  # ms: encode, forward
+    step_ms = phase.sum(axis=1)
+    ms_per_step = max_over_ranks(float(step_ms.mean()), world)
+    fl = acc.flops(B, H, N, d, w.causal)["fwd"]
+    value = world * fl / (ms_per_step * 1e-3) / 1e12
+    mean_phase = phase.mean(axis=0)
+    fwd_tf = fl / (mean_phase[1] * 1e-3) / 1e12
+    enc_gbs = acc.fp8_encode_bytes(B, H, N, d) / (mean_phase[0] * 1e-3) / 1e9
+    pk = peaks()
+    # Dense fp8 peak: the measured bf16 figure times the nominal fp8 / bf16 ratio (4.5 / 2.25).
+    peak8 = 2.0 * pk["bf16_tflops_sustained"]
+    peak8_burst = 2.0 * pk["bf16_tflops"]
+
+    pin = [t.pin_memory() for t in (x_cpu.q, x_cpu.k, x_cpu.v)]
+    outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+    e2e_steps = max(2, min(args.steps, 20))
+    dev_in = [(q, k, v), tuple(torch.empty_like(t) for t in (q, k, v))]
+    dev_out = [(o, lse), (torch.empty_like(o), torch.empty_like(lse))]
+
+    def compute(inp, out):
+        # the codes live on the compute stream only: one set serves every step
+        run(inp, out, enc)
+
+    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, compute, stream),
+                            world)
+    del dev_in, dev_out
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs = fp8_oracle_head_seconds(x_cpu, (0, 0))
+        cpu = {"value": acc.flops(1, 1, N, d, w.causal)["fwd"] / secs / 1e12, "unit": UNIT,
+               "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"one (batch, head) of {w.describe()}: NumPy e4m3 encoding + fp64 "
+                         f"forward, {secs:.1f} s; FLOPs by the same convention"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": FP8_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic",
+            "config": {"workload": w.describe(), "B": B, "H": H, "N": N, "d": d,
+                       "operands": "e4m3; power-of-two scales per 128 rows (Q, K), per head (V)",
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (402 MB of bf16 Q, K, V at the full size)",
+                       "flops_per_step": fl},
+            "pct_of_peak": value / world / peak8,
+            "timing": {"step_ms": summarize(step_ms), "encode_ms": summarize(phase[:, 0]),
+                       "fwd_ms": summarize(phase[:, 1])},
+            "phases": {"encode_gbs": enc_gbs, "fwd_kernel_tflops": fwd_tf,
+                       "hbm_peak_gbs": pk["hbm_gbs"]},
+            "roofline": {"kernel": "e4m3 forward", "bound": "tensor", "achieved": fwd_tf,
+                         "peak": peak8, "unit": "TFLOP/s", "frac": fwd_tf / peak8,
+                         "frac_of_burst": fwd_tf / peak8_burst, "traffic": None,
+                         "peak_kind": f"{pk['source']} bf16 dense sustained x 2 (nominal "
+                                      f"fp8/bf16 ratio)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * fl / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "steps": e2e_steps,
+                    "copies": "pipelined: step i+1 in and step i-1 out during step i"},
+            "gpu_launches": 6 * args.steps,
+            "clocks": clocks,
+        }, default=float), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=W.ORDER + list(W.DECODE_WORKLOADS),
+    ap.add_argument("--workload",
+                    choices=W.ORDER + list(W.DECODE_WORKLOADS) + list(W.FP8_WORKLOADS),
                     default="long_causal")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
@@ -602,10 +786,12 @@ def main():
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     world, rank, local = dist_setup()
     decode = args.workload in W.DECODE_WORKLOADS
+    fp8 = args.workload in W.FP8_WORKLOADS
     if args.impl == "reference":
-        (run_decode_reference if decode else run_reference)(args, world, rank)
+        ref = run_decode_reference if decode else run_fp8_reference if fp8 else run_reference
+        ref(args, world, rank)
     else:
-        (run_decode if decode else run_ours)(args, world, rank, local)
+        (run_decode if decode else run_fp8 if fp8 else run_ours)(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -102,3 +102,11 @@ def decode_bytes(Hq: int, Hkv: int, d: int, cache_len, elem: int = 2) -> float:
     L = float(np.asarray(cache_len, dtype=np.float64).sum())
     B = len(np.asarray(cache_len))
     return 2.0 * L * Hkv * d * elem + B * Hq * (d * elem + d * elem + 4)
+
+
+def fp8_encode_bytes(B: int, H: int, N: int, d: int) -> float:
+    """Algorithmic bytes of encoding Q, K and V to e4m3: each bf16 element read once, each
+    code written once (V^T padded to a multiple of 128 keys), plus the fp32 scales."""
+    nb = (N + BLOCK - 1) // BLOCK
+    rows = B * H * N * d
+    return 3.0 * rows * 2 + 2.0 * rows + B * H * d * nb * BLOCK + 4.0 * B * H * (2 * nb + 1)

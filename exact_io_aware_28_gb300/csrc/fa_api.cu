@@ -250,6 +250,58 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   return fa_bwd_dq_convert(dq, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream);
 }
 
+size_t fa_fp8_vt_bytes(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d) != FA_OK || d != 128) return 0;
+  return static_cast<size_t>(B) * H * d * round_up(static_cast<size_t>(N), 128);
+}
+
+namespace {
+
+fa_status check_fp8(int B, int H, int N, int d) {
+  fa_status st = fa::check_shape(B, H, N, d);
+  if (st != FA_OK) return st;
+  return d == 128 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+bool bad_scale(const float* s) { return !s || (reinterpret_cast<uintptr_t>(s) & 3u) != 0; }
+
+}  // namespace
+
+fa_status fa_fp8_quantize_qk(const void* x, void* x8, float* scale, int B, int H, int N, int d,
+                             void* stream) {
+  fa_status st = check_fp8(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (bad_ptr(x) || bad_ptr(x8) || bad_scale(scale)) return FA_ERR_INVALID_ARG;
+  return to_status(launch_fp8_quantize_rows(x, x8, scale, B * H, N,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_fp8_quantize_v(const void* v, void* vt8, float* scale, int B, int H, int N, int d,
+                            void* stream) {
+  fa_status st = check_fp8(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (bad_ptr(v) || bad_ptr(vt8) || bad_scale(scale)) return FA_ERR_INVALID_ARG;
+  return to_status(launch_fp8_quantize_v(v, vt8, scale, B * H, N,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale,
+                     const float* k_scale, const float* v_scale, void* o, float* lse,
+                     int B, int H, int N, int d, int causal, const uint8_t* blockmask,
+                     const int32_t* kv_len, float scale, void* stream) {
+  fa_status st = check_fp8(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (bad_ptr(q8) || bad_ptr(k8) || bad_ptr(vt8) || bad_ptr(o)) return FA_ERR_INVALID_ARG;
+  if (bad_scale(q_scale) || bad_scale(k_scale) || bad_scale(v_scale)) return FA_ERR_INVALID_ARG;
+  st = check_masks_scale(kv_len, lse, scale);
+  if (st != FA_OK) return st;
+  int* err = error_word();
+  if (!err) return FA_ERR_CUDA;
+  Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err, wait_limit_ns()};
+  return to_status(launch_fwd_fp8(p, q8, k8, vt8, q_scale, k_scale, v_scale, o, lse,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
 fa_status fa_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   int* err = error_word();

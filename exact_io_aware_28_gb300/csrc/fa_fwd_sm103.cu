@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include "fa_fwd_units.cuh"
 #include "fa_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -36,8 +37,8 @@ namespace fa {
 namespace {
 
 using namespace ptx;
+using namespace units;
 
-constexpr int kBlk = 128;               // rows of a Q tile / keys of a K,V tile
 constexpr int kSub = 128 * 128;         // bytes of a [128 rows][64 bf16] 128B-swizzled subtile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -66,35 +67,6 @@ struct Bars {
   int never;  // stays 0: waits that must not be cut short by an abort
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
-
-struct Unit {
-  int bh, q0, L, nb;
-};
-
-// Does query tile t (rows q0 + 128t ...) of this unit need key block j?
-__device__ __forceinline__ bool need(const Problem& p, const Unit& u, int t, int j) {
-  const int r0 = u.q0 + t * kBlk;
-  if (r0 >= p.N) return false;
-  if (j * kBlk >= u.L) return false;
-  if (p.causal && j * kBlk > r0 + kBlk - 1) return false;
-  if (p.blockmask && !p.blockmask[(r0 / kBlk) * u.nb + j]) return false;
-  return true;
-}
-
-__device__ __forceinline__ int key_blocks(const Problem& p, const Unit& u) {
-  int jend = (u.L + kBlk - 1) / kBlk;
-  if (p.causal) {
-    const int last_row = min(u.q0 + 2 * kBlk, p.N) - 1;
-    jend = min(jend, last_row / kBlk + 1);
-  }
-  return jend;
-}
-
-__device__ __forceinline__ int next_any(const Problem& p, const Unit& u, int j, int jend) {
-  for (++j; j < jend; ++j)
-    if (need(p, u, 0, j) || need(p, u, 1, j)) return j;
-  return -1;
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -478,6 +450,22 @@ bool make_head_map_rows(CUtensorMap* map, const void* ptr, int BH, int N, int d,
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [BH, rows, inner] bytes (inner contiguous) with 128 x 128 boxes and 128-byte swizzle;
+// elements outside the tensor read as zero.
+bool make_u8_map(CUtensorMap* map, const void* ptr, int BH, int rows, int inner) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(inner)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

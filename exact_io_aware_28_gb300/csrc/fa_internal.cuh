@@ -51,6 +51,19 @@ bool make_head_map(CUtensorMap* map, const void* ptr, int BH, int N, int d);
 // The same view with 64-column boxes of `box_rows` rows (1..256).
 bool make_head_map_rows(CUtensorMap* map, const void* ptr, int BH, int N, int d, int box_rows);
 
+// Tensor map of a [BH, rows, inner] byte tensor (inner contiguous, a multiple of 16) with
+// 128 x 128 boxes and 128-byte swizzle; bytes outside the tensor read as zero.
+bool make_u8_map(CUtensorMap* map, const void* ptr, int BH, int rows, int inner);
+
+// FP8 (e4m3) path, d = 128 (fa_fp8.cu): encoders and the forward.
+cudaError_t launch_fp8_quantize_rows(const void* x, void* x8, float* scale, int BH, int N,
+                                     cudaStream_t s);
+cudaError_t launch_fp8_quantize_v(const void* v, void* vt8, float* scale, int BH, int N,
+                                  cudaStream_t s);
+cudaError_t launch_fwd_fp8(const Problem& p, const void* q8, const void* k8, const void* vt8,
+                           const float* q_scale, const float* k_scale, const float* v_scale,
+                           void* o, float* lse, cudaStream_t s);
+
 // Decode over a key/value cache (split kernel + combine kernel); see fa_decode.cu.
 cudaError_t launch_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                           int B, int Hq, int Hkv, int Lmax, int d, const int32_t* cache_len,

@@ -21,7 +21,8 @@ FA_BF16, FA_FP32 = 0, 1
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_preprocess", "fa_bwd_main",
            "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_status_string", "fa_device_error",
-           "fa_selftest_wait_timeout", "fa_decode_workspace_bytes", "fa_decode")
+           "fa_selftest_wait_timeout", "fa_decode_workspace_bytes", "fa_decode",
+           "fa_fp8_vt_bytes", "fa_fp8_quantize_qk", "fa_fp8_quantize_v", "fa_fwd_fp8")
 
 # Largest workspace (bytes) fa_bwd_noalloc can serve from its built-in scratch array.
 FA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -70,6 +71,14 @@ def load() -> ctypes.CDLL:
     lib.fa_decode_workspace_bytes.restype = S
     lib.fa_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, P, F, P, S, P]
     lib.fa_decode.restype = I
+    lib.fa_fp8_vt_bytes.argtypes = [I, I, I, I]
+    lib.fa_fp8_vt_bytes.restype = S
+    lib.fa_fp8_quantize_qk.argtypes = [P, P, P, I, I, I, I, P]
+    lib.fa_fp8_quantize_qk.restype = I
+    lib.fa_fp8_quantize_v.argtypes = [P, P, P, I, I, I, I, P]
+    lib.fa_fp8_quantize_v.restype = I
+    lib.fa_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, F, P]
+    lib.fa_fwd_fp8.restype = I
     _lib = lib
     return lib
 
@@ -264,3 +273,84 @@ def decode(q, k, v, cache_len=None, scale=None, workspace=None, stream=None):
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
     fa_decode(q, k, v, o, lse, workspace, cache_len, scale, stream)
     return o, lse
+
+
+def fa_fp8_vt_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_fp8_vt_bytes(B, H, N, d))
+
+
+def _need_bf16(*ts):
+    for t in ts:
+        if t.dtype != torch.bfloat16:
+            raise TypeError("the FP8 encoders take bf16 tensors")
+
+
+def fa_fp8_quantize_qk(x, x8, scale, stream=None) -> None:
+    """x bf16 [B, H, N, 128] -> x8 uint8 [B, H, N, 128], scale fp32 [B, H, ceil(N/128)]."""
+    _check_dense(x, x8, scale)
+    _need_bf16(x)
+    B, H, N, d = x.shape
+    st = load().fa_fp8_quantize_qk(_ptr(x), _ptr(x8), _ptr(scale), B, H, N, d, _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fp8_quantize_qk")
+
+
+def fa_fp8_quantize_v(v, vt8, scale, stream=None) -> None:
+    """v bf16 [B, H, N, 128] -> vt8 uint8 [B, H, 128, Np] (opaque key order), scale [B, H]."""
+    _check_dense(v, vt8, scale)
+    _need_bf16(v)
+    B, H, N, d = v.shape
+    st = load().fa_fp8_quantize_v(_ptr(v), _ptr(vt8), _ptr(scale), B, H, N, d, _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fp8_quantize_v")
+
+
+def fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, causal=False, blockmask=None,
+               kv_len=None, scale=None, stream=None) -> None:
+    """O (bf16, preallocated) and lse of attention on e4m3-encoded inputs."""
+    _check_dense(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, blockmask, kv_len)
+    B, H, N, d = q8.shape
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    st = load().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_scale), _ptr(k_scale),
+                           _ptr(v_scale), _ptr(o), _ptr(lse), B, H, N, d, int(causal),
+                           _ptr(blockmask), _ptr(kv_len), scale, _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_fp8")
+
+
+def fp8_quantize_qk(x, stream=None):
+    """Allocate and encode: returns (x8 uint8 [B, H, N, 128], scale fp32 [B, H, nb])."""
+    B, H, N, d = x.shape
+    x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+    scale = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=x.device)
+    fa_fp8_quantize_qk(x, x8, scale, stream)
+    return x8, scale
+
+
+def fp8_quantize_v(v, stream=None):
+    """Allocate and encode: returns (vt8 uint8 [B, H, 128, Np], scale fp32 [B, H])."""
+    B, H, N, d = v.shape
+    Np = (N + 127) // 128 * 128
+    vt8 = torch.empty((B, H, d, Np), dtype=torch.uint8, device=v.device)
+    scale = torch.empty((B, H), dtype=torch.float32, device=v.device)
+    fa_fp8_quantize_v(v, vt8, scale, stream)
+    return vt8, scale
+
+
+def forward_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, causal=False, blockmask=None,
+                kv_len=None, scale=None, stream=None):
+    """Allocate o (bf16) and lse with torch and run fa_fwd_fp8."""
+    B, H, N, d = q8.shape
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, causal, blockmask, kv_len,
+               scale, stream)
+    return o, lse
+
+
+def attention_fp8(q, k, v, causal=False, blockmask=None, kv_len=None, scale=None, stream=None):
+    """bf16 q, k, v -> (o, lse) with e4m3 tensor-core products: encode, then the forward."""
+    q8, sq = fp8_quantize_qk(q, stream)
+    k8, sk = fp8_quantize_qk(k, stream)
+    vt8, sv = fp8_quantize_v(v, stream)
+    return forward_fp8(q8, k8, vt8, sq, sk, sv, causal, blockmask, kv_len, scale, stream)

@@ -72,6 +72,12 @@ WORKLOADS = {
 }
 ORDER = ["tiny_fp32", "gpt2_causal", "bert_padded", "long_causal", "block_sparse"]
 
+# The FP8 forward on the long-context shape: bf16 inputs, encoded to e4m3 on the device,
+# then the e4m3 forward (same draw as long_causal).
+FP8_WORKLOADS = {
+    "long_causal_fp8": Workload("long_causal_fp8", 1, 32, 16384, 128, "bf16", causal=True),
+}
+
 
 @dataclasses.dataclass
 class Inputs:

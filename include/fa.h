@@ -182,6 +182,39 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
                     int B, int Hq, int Hkv, int Lmax, int d, const int32_t* cache_len,
                     float scale, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * FP8 (e4m3) forward, d = 128 only (FA_ERR_UNSUPPORTED otherwise).  The pages name FP8
+ * operands as a FlashAttention-3 feature (answer page "How FlashAttention works for
+ * training", section 7; course week 13, step 2) without further detail.  Here both
+ * products take e4m3 operands on the tensor cores (tcgen05 kind::f8f6f4, fp32 accumulation);
+ * the probabilities P are rounded to e4m3 for the P V product, the row sums use them
+ * unrounded.  Encoding: x = s * e4m3(x / s) with power-of-two scales s = 2^k, k the smallest
+ * integer with max|x| <= 448 * 2^k over the scale's block (round to nearest even, saturating).
+ * Inputs must be finite.
+ *
+ * fa_fp8_quantize_qk: x bf16 [B, H, N, 128] -> x8 e4m3 bytes [B, H, N, 128] (same layout)
+ *   and scale fp32 [B, H, ceil(N / 128)], one per block of 128 rows.  For Q and K.
+ * fa_fp8_quantize_v: v bf16 [B, H, N, 128] -> vt8, e4m3 bytes of V transposed, [B, H, 128,
+ *   Np] with Np = ceil(N / 128) * 128 (fa_fp8_vt_bytes() bytes in all; columns past N are 0),
+ *   and scale fp32 [B, H], one per head.  Within each block of 128 keys, column k holds key
+ *   32(k>>5) + 16((k>>2)&1) + 8((k>>1)&1) + 2((k>>3)&3) + (k&1) of the block: the order in
+ *   which the forward's softmax threads hold P.  Treat vt8 as opaque input to fa_fwd_fp8.
+ *   Three kernels and one memset run on `stream`; `scale` is overwritten in between.
+ * fa_fwd_fp8: O and lse as fa_fwd (bf16 O [B, H, N, 128], fp32 lse [B, H, N]) of
+ *   softmax(scale Q K^T + mask) V with Q = q_scale * q8, K = k_scale * k8, V = v_scale * V8
+ *   decoded per block / per head; masks, kv_len and scale as fa_fwd.
+ * Every pointer is a device pointer; tensors 16-byte aligned, scale arrays 4-byte aligned.
+ */
+size_t fa_fp8_vt_bytes(int B, int H, int N, int d);
+fa_status fa_fp8_quantize_qk(const void* x, void* x8, float* scale, int B, int H, int N, int d,
+                             void* stream);
+fa_status fa_fp8_quantize_v(const void* v, void* vt8, float* scale, int B, int H, int N, int d,
+                            void* stream);
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale,
+                     const float* k_scale, const float* v_scale, void* o, float* lse,
+                     int B, int H, int N, int d, int causal, const uint8_t* blockmask,
+                     const int32_t* kv_len, float scale, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 

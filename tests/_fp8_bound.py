@@ -41,9 +41,12 @@ def head_terms(Q, K, V, scale, keep):
     return o, bound, var
 
 
-def check(o_lib, Q, K, V, scale, keep, rms_factor=2.0):
-    """Assert the bounds for one head; returns (max excess ratio, rms ratio)."""
-    o, bound, var = head_terms(Q, K, V, scale, keep)
+def check(o_lib, o_ref, Q, K, V, scale, keep, rms_factor=2.0):
+    """Assert the bounds for the rows of one head (Q and keep may be a subset of the rows);
+    ``o_ref`` is the oracle's exact O of those rows.  Returns (max error / bound, rms /
+    predicted rms)."""
+    _, bound, var = head_terms(Q, K, V, scale, keep)
+    o = np.asarray(o_ref, np.float64)
     diff = np.abs(np.asarray(o_lib, np.float64) - o)
     out_round = 2.0 ** -9 * (np.abs(o) + bound)
     lim = bound + out_round + 1e-7

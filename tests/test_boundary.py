@@ -18,7 +18,7 @@ pytestmark = pytest.mark.skipif(not os.path.exists(fa.LIB_PATH),
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_binding_exports():
@@ -150,3 +150,55 @@ def test_decode_workspace_bytes():
 ])
 def test_decode_rejects_bad_arguments(kw, code):
     assert dec(**kw) == code
+
+
+def test_fp8_vt_bytes():
+    assert fa.fa_fp8_vt_bytes(1, 2, 300, 128) == 2 * 128 * 384
+    assert fa.fa_fp8_vt_bytes(1, 32, 16384, 128) == 32 * 128 * 16384
+    assert fa.fa_fp8_vt_bytes(1, 2, 300, 64) == 0      # d = 128 only
+    assert fa.fa_fp8_vt_bytes(1, 2, 0, 128) == 0
+
+
+def fwd8(**kw):
+    args = dict(q8=A, k8=A, vt8=A, sq=A, sk=A, sv=A, o=A, lse=A, B=1, H=2, N=300, d=128,
+                causal=1, bm=None, kv=None, scale=0.088)
+    args.update(kw)
+    return fa.load().fa_fwd_fp8(args["q8"], args["k8"], args["vt8"], args["sq"], args["sk"],
+                                args["sv"], args["o"], args["lse"], args["B"], args["H"],
+                                args["N"], args["d"], args["causal"], args["bm"], args["kv"],
+                                args["scale"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"q8": None}, fa.FA_ERR_INVALID_ARG),
+    ({"vt8": A + 8}, fa.FA_ERR_INVALID_ARG),
+    ({"o": A + 2}, fa.FA_ERR_INVALID_ARG),
+    ({"sq": None}, fa.FA_ERR_INVALID_ARG),
+    ({"sk": A + 2}, fa.FA_ERR_INVALID_ARG),
+    ({"sv": None}, fa.FA_ERR_INVALID_ARG),
+    ({"lse": None}, fa.FA_ERR_INVALID_ARG),
+    ({"kv": A + 1}, fa.FA_ERR_INVALID_ARG),
+    ({"d": 64}, fa.FA_ERR_UNSUPPORTED),
+    ({"N": 0}, fa.FA_ERR_INVALID_ARG),
+    ({"scale": 0.0}, fa.FA_ERR_INVALID_ARG),
+    ({"scale": float("inf")}, fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_fp8_rejects_bad_arguments(kw, code):
+    assert fwd8(**kw) == code
+
+
+@pytest.mark.parametrize("fn", ["fa_fp8_quantize_qk", "fa_fp8_quantize_v"])
+@pytest.mark.parametrize("kw,code", [
+    ({"x": None}, fa.FA_ERR_INVALID_ARG),
+    ({"x8": A + 4}, fa.FA_ERR_INVALID_ARG),
+    ({"s": None}, fa.FA_ERR_INVALID_ARG),
+    ({"s": A + 2}, fa.FA_ERR_INVALID_ARG),
+    ({"d": 64}, fa.FA_ERR_UNSUPPORTED),
+    ({"H": 0}, fa.FA_ERR_INVALID_ARG),
+])
+def test_fp8_encoders_reject_bad_arguments(fn, kw, code):
+    args = dict(x=A, x8=A, s=A, B=1, H=2, N=300, d=128)
+    args.update(kw)
+    f = getattr(fa.load(), fn)
+    assert f(args["x"], args["x8"], args["s"], args["B"], args["H"], args["N"], args["d"],
+             None) == code

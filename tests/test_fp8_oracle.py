@@ -121,7 +121,8 @@ def test_p_rounding_bound_covers_an_emulation_of_the_kernel(shift):
         lk = Pk.sum(axis=1, dtype=np.float32)
         Pq = fp8.e4m3_round(Pk.astype(np.float64))
         o_emu = (Pq @ V) / lk[:, None]
-        worst, rms_ratio = _fp8_bound.check(o_emu, Q, K, V, scale, keep)
+        o_ref = oracle.forward_head(Q, K, V, scale, keep)[0]
+        worst, rms_ratio = _fp8_bound.check(o_emu, o_ref, Q, K, V, scale, keep)
         assert worst <= 1.0 and rms_ratio <= 2.0
 
 
@@ -135,5 +136,6 @@ def test_p_rounding_bound_detects_a_permuted_value_block():
     perm = np.arange(N)
     perm[0:32], perm[32:64] = np.arange(32, 64), np.arange(0, 32)
     o_bad, _, _ = _fp8_bound.head_terms(Q, K, V[perm], scale, keep)
+    o_ref = oracle.forward_head(Q, K, V, scale, keep)[0]
     with pytest.raises(AssertionError):
-        _fp8_bound.check(o_bad, Q, K, V, scale, keep)
+        _fp8_bound.check(o_bad, o_ref, Q, K, V, scale, keep)
