@@ -2,7 +2,8 @@
 """Benchmark: exact attention forward + backward on GB300 through the C ABI.
 
 One step = fa_fwd + the three backward stages (preprocess, main, dQ convert) over one
-batch of seeded synthetic input already resident in HBM.  Prints ONE JSON line (rank 0).
+batch of seeded synthetic input already resident in HBM (with dropout: fa_fwd_dropout and
+fa_bwd_main_dropout in place of fa_fwd and fa_bwd_main).  Prints ONE JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long_causal]
     python bench.py --impl reference ...   # the CPU fp64 oracle on a bounded sample
@@ -38,6 +39,8 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 # Kernels launched per step by the library (fwd, preprocess, main, dQ convert).
 KERNELS_PER_STEP = {"bf16": 4, "fp32": 4}
+# Training-step workloads: the five plain ones and the one with attention dropout.
+TRAIN_WORKLOADS = {**W.WORKLOADS, **W.DROPOUT_WORKLOADS}
 
 
 def peaks() -> dict:
@@ -136,8 +139,9 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def oracle_head_seconds(x, head) -> float:
-    """Run the oracle's forward and backward on one (b, h) head; return wall seconds."""
+def oracle_head_seconds(x, head, w=None) -> float:
+    """Run the oracle's forward and backward on one (b, h) head; return wall seconds.
+    With a dropout workload the mask generation is part of the timed work."""
     import oracle
     b, h = head
     q, k, v, do = (t[b, h].to(torch.float64).numpy() for t in (x.q, x.k, x.v, x.do))
@@ -145,8 +149,14 @@ def oracle_head_seconds(x, head) -> float:
     kl = None if x.kv_len is None else int(x.kv_len[b])
     keep = oracle.keep_mask(q.shape[0], x.causal, bm, kl)
     t0 = time.perf_counter()
-    oracle.forward_head(q, k, v, x.scale, keep)
-    oracle.backward_head(q, k, v, do, x.scale, keep)
+    if w is not None and w.drop_threshold:
+        dr = oracle.dropout
+        z = dr.keep_drop_mask(w.drop_seed, 0, b * x.q.shape[1] + h, q.shape[0], w.drop_threshold)
+        dr.forward_head(q, k, v, x.scale, keep, z, w.drop_threshold)
+        dr.backward_head(q, k, v, do, x.scale, keep, z, w.drop_threshold)
+    else:
+        oracle.forward_head(q, k, v, x.scale, keep)
+        oracle.backward_head(q, k, v, do, x.scale, keep)
     return time.perf_counter() - t0
 
 
@@ -163,7 +173,7 @@ def cpu_cores() -> int:
 
 
 def cpu_baseline(w: W.Workload, x_cpu) -> dict:
-    secs = oracle_head_seconds(x_cpu, (0, 0))
+    secs = oracle_head_seconds(x_cpu, (0, 0), w)
     return {"value": head_flops(w, x_cpu) / secs / 1e12, "unit": UNIT, "cores": cpu_cores(),
             "kind": "oracle",
             "sample": f"one (batch, head) of {w.describe()}: fp64 NumPy forward + backward, "
@@ -174,16 +184,16 @@ def run_reference(args, world, rank):
     """The CPU fp64 oracle as it stands: one (batch, head) of the workload per step."""
     if rank != 0:
         return
-    w = W.WORKLOADS[args.workload]
+    w = TRAIN_WORKLOADS[args.workload]
     x = W.make_inputs(w, seed=0)
     small = W.make_inputs(W.custom("warm", 1, 1, 256, w.d, w.dtype, causal=w.causal), seed=1)
     for _ in range(args.warmup):
-        oracle_head_seconds(small, (0, 0))
+        oracle_head_seconds(small, (0, 0), w)
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     # A long-sequence head takes seconds in fp64: time at most 20 of the requested steps so
     # that the whole run stays within a few minutes, and say so in the line.
     timed = max(1, min(args.steps, 20))
-    times = [oracle_head_seconds(x, heads[i % len(heads)]) for i in range(timed)]
+    times = [oracle_head_seconds(x, heads[i % len(heads)], w) for i in range(timed)]
     mean = sum(times) / len(times)
     value = head_flops(w, x) / mean / 1e12
     line = {
@@ -265,7 +275,7 @@ def run_ours(args, world, rank, local):
     from exact_io_aware_28_gb300 import fa
 
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = W.WORKLOADS[args.workload]
+    w = TRAIN_WORKLOADS[args.workload]
     if args.heads:
         w = dataclasses.replace(w, H=args.heads)
     x_cpu = W.make_inputs(w, seed=0)
@@ -287,18 +297,33 @@ def run_ours(args, world, rank, local):
     flush = in_bytes < 2 * L2_BYTES
     scratch = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
     stream = torch.cuda.current_stream()
+    drop = (w.drop_threshold, w.drop_seed, 0)
+
+    def fwd_call(q_, k_, v_, o_, lse_):
+        if w.drop_threshold:
+            fa.fa_fwd_dropout(q_, k_, v_, o_, lse_, *drop, x.causal, x.blockmask, x.kv_len,
+                              x.scale, stream)
+        else:
+            fa.fa_fwd(q_, k_, v_, o_, lse_, x.causal, x.blockmask, x.kv_len, x.scale, stream)
+
+    def main_call(q_, k_, v_, lse_, do_, dq_, dk_, dv_):
+        if w.drop_threshold:
+            fa.fa_bwd_main_dropout(q_, k_, v_, lse_, do_, dq_, dk_, dv_, ws, *drop, x.causal,
+                                   x.blockmask, x.kv_len, x.scale, stream)
+        else:
+            fa.fa_bwd_main(q_, k_, v_, lse_, do_, dq_, dk_, dv_, ws, x.causal, x.blockmask,
+                           x.kv_len, x.scale, stream)
 
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        fa.fa_fwd(x.q, x.k, x.v, o, lse, x.causal, x.blockmask, x.kv_len, x.scale, stream)
+        fwd_call(x.q, x.k, x.v, o, lse)
         if ev:
             ev[1].record(stream)
         fa.fa_bwd_preprocess(o, x.do, ws, stream)
         if ev:
             ev[2].record(stream)
-        fa.fa_bwd_main(x.q, x.k, x.v, lse, x.do, dq, dk, dv, ws, x.causal, x.blockmask,
-                       x.kv_len, x.scale, stream)
+        main_call(x.q, x.k, x.v, lse, x.do, dq, dk, dv)
         if ev:
             ev[3].record(stream)
         fa.fa_bwd_dq_convert(dq, ws, x.scale, stream)
@@ -379,10 +404,9 @@ def run_ours(args, world, rank, local):
     def compute(inp, out):
         q_, k_, v_, do_ = inp
         o_, lse_, dq_, dk_, dv_ = out
-        fa.fa_fwd(q_, k_, v_, o_, lse_, x.causal, x.blockmask, x.kv_len, x.scale, stream)
+        fwd_call(q_, k_, v_, o_, lse_)
         fa.fa_bwd_preprocess(o_, do_, ws, stream)
-        fa.fa_bwd_main(q_, k_, v_, lse_, do_, dq_, dk_, dv_, ws, x.causal, x.blockmask,
-                       x.kv_len, x.scale, stream)
+        main_call(q_, k_, v_, lse_, do_, dq_, dk_, dv_)
         fa.fa_bwd_dq_convert(dq_, ws, x.scale, stream)
 
     e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, compute, stream),
@@ -774,7 +798,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload",
-                    choices=W.ORDER + list(W.DECODE_WORKLOADS) + list(W.FP8_WORKLOADS),
+                    choices=W.ORDER + list(W.DROPOUT_WORKLOADS) + list(W.DECODE_WORKLOADS) +
+                    list(W.FP8_WORKLOADS),
                     default="long_causal")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,

@@ -121,10 +121,25 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   return round_up(rows * sizeof(float), 256) + rows * (size_t)d * sizeof(float);
 }
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                 int B, int H, int N, int d, int causal,
-                 const uint8_t* blockmask, const int32_t* kv_len,
-                 float scale, fa_dtype dtype, void* stream) {
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+// Dropout arguments as the kernels take them; threshold 0 is no dropout.
+void set_dropout(Problem* p, int threshold, uint64_t seed, uint32_t offset) {
+  p->drop_threshold = threshold;
+  p->drop_seed_lo = static_cast<uint32_t>(seed);
+  p->drop_seed_hi = static_cast<uint32_t>(seed >> 32);
+  p->drop_offset = offset;
+  p->drop_scale = 256.f / static_cast<float>(256 - threshold);
+}
+
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, int causal,
+                   const uint8_t* blockmask, const int32_t* kv_len,
+                   float scale, fa_dtype dtype, void* stream,
+                   int drop_threshold, uint64_t seed, uint32_t offset) {
   fa_status st = check_shape(B, H, N, d);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
@@ -136,10 +151,34 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   int* err = error_word();
   if (!err) return FA_ERR_CUDA;
   Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err, wait_limit_ns()};
+  set_dropout(&p, drop_threshold, seed, offset);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == FA_BF16 ? launch_fwd_sm103(p, q, k, v, o, lse, s)
                                    : launch_fwd_simt(p, dtype, q, k, v, o, lse, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, int causal,
+                 const uint8_t* blockmask, const int32_t* kv_len,
+                 float scale, fa_dtype dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, blockmask, kv_len, scale, dtype, stream,
+                  0, 0, 0);
+}
+
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, int causal,
+                         const uint8_t* blockmask, const int32_t* kv_len,
+                         float scale, fa_dtype dtype, int drop_threshold,
+                         unsigned long long seed, unsigned int offset, void* stream) {
+  if (drop_threshold < 0 || drop_threshold > 255) return FA_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, blockmask, kv_len, scale, dtype, stream,
+                  drop_threshold, seed, offset);
 }
 
 namespace {
@@ -194,12 +233,17 @@ fa_status fa_bwd_preprocess(const void* o, const void* dO, int B, int H, int N, 
                                          static_cast<cudaStream_t>(stream)));
 }
 
-fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* lse,
-                      const void* dO, void* dq, void* dk, void* dv,
-                      int B, int H, int N, int d, int causal,
-                      const uint8_t* blockmask, const int32_t* kv_len,
-                      float scale, fa_dtype dtype,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status bwd_main_impl(const void* q, const void* k, const void* v, const float* lse,
+                        const void* dO, void* dq, void* dk, void* dv,
+                        int B, int H, int N, int d, int causal,
+                        const uint8_t* blockmask, const int32_t* kv_len,
+                        float scale, fa_dtype dtype,
+                        void* workspace, size_t workspace_bytes, void* stream,
+                        int drop_threshold, uint64_t seed, uint32_t offset) {
   fa_status st = check_common(B, H, N, d, dtype, workspace, workspace_bytes);
   if (st != FA_OK) return st;
   if (bad_ptr(q) || bad_ptr(k) || bad_ptr(v) || bad_ptr(dO) || bad_ptr(dk) || bad_ptr(dv))
@@ -210,11 +254,61 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* 
   int* err = fa::error_word();
   if (!err) return FA_ERR_CUDA;
   Problem p{B, H, N, d, causal ? 1 : 0, blockmask, kv_len, scale, err, wait_limit_ns()};
+  fa::set_dropout(&p, drop_threshold, seed, offset);
   Workspace w = carve(workspace, B, H, N);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == FA_BF16)
     return to_status(launch_bwd_sm103(p, q, k, v, lse, dO, w.Dsum, w.dq_acc, dk, dv, s));
   return to_status(launch_bwd_simt(p, dtype, q, k, v, lse, dO, w.Dsum, dq, dk, dv, s));
+}
+
+fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv,
+                   int B, int H, int N, int d, int causal,
+                   const uint8_t* blockmask, const int32_t* kv_len,
+                   float scale, fa_dtype dtype,
+                   void* workspace, size_t workspace_bytes, void* stream,
+                   int drop_threshold, uint64_t seed, uint32_t offset) {
+  fa_status st = check_common(B, H, N, d, dtype, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  if (bad_ptr(q) || bad_ptr(k) || bad_ptr(v) || bad_ptr(o) || bad_ptr(dO) || bad_ptr(dq) ||
+      bad_ptr(dk) || bad_ptr(dv))
+    return FA_ERR_INVALID_ARG;
+  st = check_masks_scale(kv_len, lse, scale);
+  if (st != FA_OK) return st;
+  st = fa_bwd_preprocess(o, dO, B, H, N, d, dtype, workspace, workspace_bytes, stream);
+  if (st != FA_OK) return st;
+  st = bwd_main_impl(q, k, v, lse, dO, dq, dk, dv, B, H, N, d, causal, blockmask, kv_len, scale,
+                     dtype, workspace, workspace_bytes, stream, drop_threshold, seed, offset);
+  if (st != FA_OK) return st;
+  return fa_bwd_dq_convert(dq, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* lse,
+                      const void* dO, void* dq, void* dk, void* dv,
+                      int B, int H, int N, int d, int causal,
+                      const uint8_t* blockmask, const int32_t* kv_len,
+                      float scale, fa_dtype dtype,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_main_impl(q, k, v, lse, dO, dq, dk, dv, B, H, N, d, causal, blockmask, kv_len,
+                       scale, dtype, workspace, workspace_bytes, stream, 0, 0, 0);
+}
+
+fa_status fa_bwd_main_dropout(const void* q, const void* k, const void* v, const float* lse,
+                              const void* dO, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, int causal,
+                              const uint8_t* blockmask, const int32_t* kv_len,
+                              float scale, fa_dtype dtype, int drop_threshold,
+                              unsigned long long seed, unsigned int offset,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (drop_threshold < 0 || drop_threshold > 255) return FA_ERR_INVALID_ARG;
+  return bwd_main_impl(q, k, v, lse, dO, dq, dk, dv, B, H, N, d, causal, blockmask, kv_len,
+                       scale, dtype, workspace, workspace_bytes, stream, drop_threshold, seed,
+                       offset);
 }
 
 fa_status fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, float scale, fa_dtype dtype,
@@ -235,19 +329,30 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const uint8_t* blockmask, const int32_t* kv_len,
                  float scale, fa_dtype dtype,
                  void* workspace, size_t workspace_bytes, void* stream) {
-  fa_status st = check_common(B, H, N, d, dtype, workspace, workspace_bytes);
-  if (st != FA_OK) return st;
-  if (bad_ptr(q) || bad_ptr(k) || bad_ptr(v) || bad_ptr(o) || bad_ptr(dO) || bad_ptr(dq) ||
-      bad_ptr(dk) || bad_ptr(dv))
-    return FA_ERR_INVALID_ARG;
-  st = check_masks_scale(kv_len, lse, scale);
-  if (st != FA_OK) return st;
-  st = fa_bwd_preprocess(o, dO, B, H, N, d, dtype, workspace, workspace_bytes, stream);
-  if (st != FA_OK) return st;
-  st = fa_bwd_main(q, k, v, lse, dO, dq, dk, dv, B, H, N, d, causal, blockmask, kv_len, scale,
-                   dtype, workspace, workspace_bytes, stream);
-  if (st != FA_OK) return st;
-  return fa_bwd_dq_convert(dq, B, H, N, d, scale, dtype, workspace, workspace_bytes, stream);
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, blockmask, kv_len, scale,
+                  dtype, workspace, workspace_bytes, stream, 0, 0, 0);
+}
+
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, int causal,
+                         const uint8_t* blockmask, const int32_t* kv_len,
+                         float scale, fa_dtype dtype, int drop_threshold,
+                         unsigned long long seed, unsigned int offset,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (drop_threshold < 0 || drop_threshold > 255) return FA_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, blockmask, kv_len, scale,
+                  dtype, workspace, workspace_bytes, stream, drop_threshold, seed, offset);
+}
+
+fa_status fa_dropout_random_bytes(void* out, int BH, int n_q, int n_k, unsigned long long seed,
+                                  unsigned int offset, void* stream) {
+  if (!out || BH < 1 || n_q < 1 || n_k < 1 || BH > 65535) return FA_ERR_INVALID_ARG;
+  if ((long long)n_q * n_k > (1ll << 31)) return FA_ERR_UNSUPPORTED;
+  Problem p{1, BH, n_q, 64, 0, nullptr, nullptr, 1.f, nullptr, 0};
+  set_dropout(&p, 0, seed, offset);
+  return to_status(launch_dropout_bytes(p, static_cast<uint8_t*>(out), BH, n_q, n_k,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 size_t fa_fp8_vt_bytes(int B, int H, int N, int d) {

@@ -39,6 +39,7 @@
 #include <math.h>
 
 #include "fa_internal.cuh"
+#include "fa_philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -113,7 +114,9 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
          ((col & 7) << 1);
 }
 
-template <int D>
+// DROP: dropout on P, its mask regenerated from the generator of fa_philox.cuh: dV takes
+// P o Z (scaled by 1 / (1 - p) in the epilogue), dS = P o (Z o dP / (1 - p) - D).
+template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -358,6 +361,26 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       if (!ok) break;
       const bool diag = p.causal && i == u.j;
       const int lim = diag ? r : 0;   // diagonal block: query column q sees key r iff q >= r
+      // Dropout: bit x of zbits keeps element (query 128 i + 64 w + x, this key row).  Query
+      // rows x and x + 8 (x % 16 < 8) share a generator call; this key's bytes sit in word
+      // (key >> 3) & 3, at byte (key & 1) for row x and 2 + (key & 1) for row x + 8.
+      uint64_t zbits = 0;
+      if constexpr (DROP) {
+        const uint32_t octet = philox::key_octet(key), cw = (key >> 3) & 3;
+        const uint32_t sh = 8u * (key & 1);
+        const uint32_t thr = static_cast<uint32_t>(p.drop_threshold);
+#pragma unroll 4
+        for (int x2 = 0; x2 < 32; ++x2) {
+          const int x = 16 * (x2 >> 3) + (x2 & 7);
+          const philox::Words g = philox::philox4x32_10(
+              octet, philox::row_pair(i * kBlk + 64 * w + x), static_cast<uint32_t>(u.bh),
+              p.drop_offset, p.drop_seed_lo, p.drop_seed_hi);
+          const uint32_t wd = cw == 0 ? g.w[0] : cw == 1 ? g.w[1] : cw == 2 ? g.w[2] : g.w[3];
+          const uint64_t k0 = ((wd >> sh) & 0xFFu) >= thr ? 1ull : 0ull;
+          const uint64_t k1 = ((wd >> (sh + 16)) & 0xFFu) >= thr ? 1ull : 0ull;
+          zbits |= (k0 << x) | (k1 << (x + 8));
+        }
+      }
       // ---- phase A: P^T = exp2(S^T * c - lse * log2 e) for this warpgroup's 64 columns
       ok = mbar_wait_warp(&bars->s_full, n & 1, abort_flag, p.err, p.wait_ns);
       if (!ok) break;
@@ -395,7 +418,18 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
       }
       // P^T over this warpgroup's own, already-read S^T columns [64w, 64w + 32).
-      tmem_st32(lane_base + 64 * w, pp);
+      if constexpr (DROP) {
+        // dV takes P o Z; phase B still needs P itself.
+        uint32_t pz[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const uint32_t b = static_cast<uint32_t>(zbits >> (2 * e)) & 3u;
+          pz[e] = pp[e] & ((b & 1u ? 0x0000FFFFu : 0u) | (b & 2u ? 0xFFFF0000u : 0u));
+        }
+        tmem_st32(lane_base + 64 * w, pz);
+      } else {
+        tmem_st32(lane_base + 64 * w, pp);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
@@ -423,10 +457,25 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           const float4 nd = dvals[e4];   // -D
           const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * h + 2 * e4]));
           const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * h + 2 * e4 + 1]));
-          const float2 d01 = f2_unpack(fmul2(f2_pack(p01.x, p01.y),
-              fadd2(f2_pack(__uint_as_float(dpv[4 * e4 + 0]), __uint_as_float(dpv[4 * e4 + 1])), f2_pack(nd.x, nd.y))));
-          const float2 d23 = f2_unpack(fmul2(f2_pack(p23.x, p23.y),
-              fadd2(f2_pack(__uint_as_float(dpv[4 * e4 + 2]), __uint_as_float(dpv[4 * e4 + 3])), f2_pack(nd.z, nd.w))));
+          float2 d01, d23;
+          if constexpr (DROP) {
+            // dS = P o (Z o dP / (1 - p) - D)
+            const int x = 32 * h + 4 * e4;
+            const float ks = p.drop_scale;
+            const float z0 = (zbits >> x) & 1 ? ks : 0.f, z1 = (zbits >> (x + 1)) & 1 ? ks : 0.f;
+            const float z2 = (zbits >> (x + 2)) & 1 ? ks : 0.f, z3 = (zbits >> (x + 3)) & 1 ? ks : 0.f;
+            d01 = f2_unpack(fmul2(f2_pack(p01.x, p01.y),
+                ffma2(f2_pack(__uint_as_float(dpv[4 * e4 + 0]), __uint_as_float(dpv[4 * e4 + 1])),
+                      f2_pack(z0, z1), f2_pack(nd.x, nd.y))));
+            d23 = f2_unpack(fmul2(f2_pack(p23.x, p23.y),
+                ffma2(f2_pack(__uint_as_float(dpv[4 * e4 + 2]), __uint_as_float(dpv[4 * e4 + 3])),
+                      f2_pack(z2, z3), f2_pack(nd.z, nd.w))));
+          } else {
+            d01 = f2_unpack(fmul2(f2_pack(p01.x, p01.y),
+                fadd2(f2_pack(__uint_as_float(dpv[4 * e4 + 0]), __uint_as_float(dpv[4 * e4 + 1])), f2_pack(nd.x, nd.y))));
+            d23 = f2_unpack(fmul2(f2_pack(p23.x, p23.y),
+                fadd2(f2_pack(__uint_as_float(dpv[4 * e4 + 2]), __uint_as_float(dpv[4 * e4 + 3])), f2_pack(nd.z, nd.w))));
+          }
           dsp[2 * e4] = pack_bf16x2(d01.x, d01.y);
           dsp[2 * e4 + 1] = pack_bf16x2(d23.x, d23.y);
         }
@@ -452,7 +501,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     // TMEM loads are warp-collective: every lane loads, only rows inside the sequence store.
     if (ok) {
       const bool store = key < p.N;
-      const float mul = w == 0 ? p.scale : 1.f;
+      const float mul = w == 0 ? p.scale : (DROP ? p.drop_scale : 1.f);
       __nv_bfloat16* dst = (w == 0 ? dk : dv) + (row_off + key) * D;
       const uint32_t col0 = w == 0 ? 384u : 256u;
 #pragma unroll 1
@@ -555,7 +604,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 cudaError_t bwd_launch(const Problem& p, const void* q, const void* k, const void* v,
                        const float* lse, const void* dO, const float* Dsum, float* dq_acc,
                        void* dk, void* dv, cudaStream_t s) {
@@ -569,14 +618,14 @@ cudaError_t bwd_launch(const Problem& p, const void* q, const void* k, const voi
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_sm103_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_sm103_kernel<D, DROP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int nkb = (p.N + kBlk - 1) / kBlk;
   dim3 grid(static_cast<unsigned>(BH) * nkb);
-  bwd_sm103_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, s>>>(
+  bwd_sm103_kernel<D, DROP><<<grid, kThreads, Cfg<D>::SMEM, s>>>(
       mq, mk, mv, mdo, mdq, lse, Dsum, dq_acc, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), p);
   return cudaGetLastError();
@@ -587,8 +636,11 @@ cudaError_t bwd_launch(const Problem& p, const void* q, const void* k, const voi
 cudaError_t launch_bwd_sm103(const Problem& p, const void* q, const void* k, const void* v,
                              const float* lse, const void* dO, const float* Dsum, float* dq_acc,
                              void* dk, void* dv, cudaStream_t s) {
-  return p.d == 64 ? bwd_launch<64>(p, q, k, v, lse, dO, Dsum, dq_acc, dk, dv, s)
-                   : bwd_launch<128>(p, q, k, v, lse, dO, Dsum, dq_acc, dk, dv, s);
+  if (p.drop_threshold > 0)
+    return p.d == 64 ? bwd_launch<64, true>(p, q, k, v, lse, dO, Dsum, dq_acc, dk, dv, s)
+                     : bwd_launch<128, true>(p, q, k, v, lse, dO, Dsum, dq_acc, dk, dv, s);
+  return p.d == 64 ? bwd_launch<64, false>(p, q, k, v, lse, dO, Dsum, dq_acc, dk, dv, s)
+                   : bwd_launch<128, false>(p, q, k, v, lse, dO, Dsum, dq_acc, dk, dv, s);
 }
 
 }  // namespace fa

@@ -31,6 +31,7 @@
 
 #include "fa_fwd_units.cuh"
 #include "fa_internal.cuh"
+#include "fa_philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -68,7 +69,8 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-template <int D>
+// DROP: dropout on P (the generator bytes of fa_philox.cuh); the row sums keep every term.
+template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
@@ -314,8 +316,22 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         const uint64_t nA = f2_pack(-useA, -useA), nB = f2_pack(-useB, -useB);
         uint64_t accA = f2_pack(0.f, 0.f), accB = accA;
         uint32_t pk[32];
+        philox::Words keep{};
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
+          if constexpr (DROP) {
+            // One generator call per four key chunks: word cc % 4 holds the bytes of keys
+            // 8cc + 2(t % 4) + {0, 1} of rows A and B, in that order.
+            if ((cc & 3) == 0) {
+              keep = philox::philox4x32_10(
+                  static_cast<uint32_t>(4 * (4 * j + (cc >> 2)) + t4),
+                  philox::row_pair(u.q0 + t * kBlk + rA), static_cast<uint32_t>(u.bh),
+                  p.drop_offset, p.drop_seed_lo, p.drop_seed_hi);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                keep.w[k] = philox::keep_bytes(keep.w[k], 0x01010101u * p.drop_threshold);
+            }
+          }
           const float2 xa = f2_unpack(ffma2(f2_pack(sv[4 * cc], sv[4 * cc + 1]), c2, nA));
           const float2 xb = f2_unpack(ffma2(f2_pack(sv[4 * cc + 2], sv[4 * cc + 3]), c2, nB));
           const float pa0 = ex2(xa.x), pa1 = ex2(xa.y);
@@ -324,6 +340,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           accB = fadd2(accB, f2_pack(pb0, pb1));
           pk[2 * cc] = pack_bf16x2(pa0, pa1);
           pk[2 * cc + 1] = pack_bf16x2(pb0, pb1);
+          if constexpr (DROP) {  // dropped probabilities leave P V but not the row sums
+            pk[2 * cc] &= __byte_perm(keep.w[cc & 3], 0u, 0x1100);
+            pk[2 * cc + 1] &= __byte_perm(keep.w[cc & 3], 0u, 0x3322);
+          }
         }
         // P (bf16 pairs) overwrites the first 64 columns of this tile's S region in this
         // warp's 16 lanes, which no other warp reads; the load above has completed.
@@ -365,7 +385,11 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       lB += __shfl_xor_sync(0xffffffffu, lB, 1);
       lA += __shfl_xor_sync(0xffffffffu, lA, 2);
       lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-      const float invA = lA > 0.f ? 1.f / lA : 0.f, invB = lB > 0.f ? 1.f / lB : 0.f;
+      float invA = lA > 0.f ? 1.f / lA : 0.f, invB = lB > 0.f ? 1.f / lB : 0.f;
+      if constexpr (DROP) {
+        invA *= p.drop_scale;
+        invB *= p.drop_scale;
+      }
       const int rowA = u.q0 + t * kBlk + rA, rowB = rowA + 8;
       // O / l as bf16 into this tile's Q buffer (every S MMA that read it has completed: they
       // precede the last P V product of this tile), in the 128-byte-swizzled layout of the
@@ -490,7 +514,7 @@ bool make_acc_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool DROP>
 static cudaError_t fwd_launch(const Problem& p, const void* q, const void* k, const void* v,
                               void* o, float* lse, cudaStream_t s) {
   CUtensorMap mq, mk, mv, mo;
@@ -502,21 +526,24 @@ static cudaError_t fwd_launch(const Problem& p, const void* q, const void* k, co
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, DROP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int nqb = (p.N + 255) / 256;
   dim3 grid(static_cast<unsigned>(BH) * nqb);
-  fwd_sm103_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, s>>>(mq, mk, mv, mo, lse, p);
+  fwd_sm103_kernel<D, DROP><<<grid, kThreads, Cfg<D>::SMEM, s>>>(mq, mk, mv, mo, lse, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_sm103(const Problem& p, const void* q, const void* k, const void* v,
                              void* o, float* lse, cudaStream_t s) {
-  return p.d == 64 ? fwd_launch<64>(p, q, k, v, o, lse, s)
-                   : fwd_launch<128>(p, q, k, v, o, lse, s);
+  if (p.drop_threshold > 0)
+    return p.d == 64 ? fwd_launch<64, true>(p, q, k, v, o, lse, s)
+                     : fwd_launch<128, true>(p, q, k, v, o, lse, s);
+  return p.d == 64 ? fwd_launch<64, false>(p, q, k, v, o, lse, s)
+                   : fwd_launch<128, false>(p, q, k, v, o, lse, s);
 }
 
 }  // namespace fa

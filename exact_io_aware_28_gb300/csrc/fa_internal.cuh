@@ -22,6 +22,11 @@ struct Problem {
   float scale;
   int* err;                  // device error word
   unsigned long long wait_ns;  // bound of every mbarrier wait in the tensor-core kernels
+  // Dropout on the probabilities (threshold 0: none): element (bh, i, j) is dropped when its
+  // generator byte is below drop_threshold, kept ones are scaled by drop_scale.
+  int drop_threshold = 0;
+  uint32_t drop_seed_lo = 0, drop_seed_hi = 0, drop_offset = 0;
+  float drop_scale = 1.f;    // 256 / (256 - drop_threshold)
 };
 
 // Bound of device-side waits: FA_WAIT_LIMIT_MS from the environment (read once), else 2 s.
@@ -44,6 +49,10 @@ cudaError_t launch_fwd_sm103(const Problem& p, const void* q, const void* k, con
 cudaError_t launch_bwd_sm103(const Problem& p, const void* q, const void* k, const void* v,
                              const float* lse, const void* dO, const float* D, float* dq_acc,
                              void* dk, void* dv, cudaStream_t s);
+
+// Generator bytes of dropout for [BH, n_q, n_k] elements (fa_dropout.cu).
+cudaError_t launch_dropout_bytes(const Problem& p, uint8_t* out, int BH, int n_q, int n_k,
+                                 cudaStream_t s);
 
 // Tensor map of a [B*H, N, d] bf16 tensor (d innermost) with 64 x 128 boxes and 128-byte
 // swizzle; rows beyond N read as zero.  Returns false if the driver rejects it.

@@ -14,11 +14,17 @@
 // Scores are kept in the log2 domain (q pre-multiplied by scale*log2(e)) so that every
 // exponential is an exp2.
 //
+// Dropout (threshold > 0): the probability of element (i, j) enters P V, dV and dP as
+// P_ij Z_ij / (1 - p), with Z regenerated from the generator of fa_philox.cuh in each
+// kernel; the row sums of the forward keep every term.  One generator call per element
+// (this path serves small problems).
+//
 // Thread layout: four threads per row, each owning every fourth element of the head
 // dimension; dot products finish with two xor-shuffles inside the group of four.
 #include <math.h>
 
 #include "fa_internal.cuh"
+#include "fa_philox.cuh"
 
 namespace fa {
 namespace {
@@ -45,6 +51,15 @@ __device__ __forceinline__ int key_limit(const Problem& p, int b) {
   if (!p.kv_len) return p.N;
   int L = p.kv_len[b];
   return L < 0 ? 0 : (L > p.N ? p.N : L);
+}
+
+// Z_ij / (1 - p) of element (bh, i, j): 0 when dropped, the keep scale otherwise (1 with
+// no dropout).
+__device__ __forceinline__ float drop_factor(const Problem& p, int bh, int i, int j) {
+  if (p.drop_threshold <= 0) return 1.f;
+  const philox::Words g = philox::call(p, bh, i, j);
+  return philox::byte_of(g, i, j) >= static_cast<uint32_t>(p.drop_threshold) ? p.drop_scale
+                                                                               : 0.f;
 }
 
 __device__ __forceinline__ float group_sum(float x) {
@@ -107,12 +122,13 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
       }
       const float pj = exp2f(s - m);
       l += pj;
+      const float pz = pj * drop_factor(p, bh, row, key);
 #pragma unroll
-      for (int t = 0; t < DS; ++t) acc[t] += pj * vs[j][part + kTPR * t];
+      for (int t = 0; t < DS; ++t) acc[t] += pz * vs[j][part + kTPR * t];
     }
   }
   if (valid_row) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? 1.f / l : 0.f;   // dropout's 1 / (1 - p) is in drop_factor
 #pragma unroll
     for (int t = 0; t < DS; ++t) o[head + (size_t)row * D + part + kTPR * t] = from_f<T>(acc[t] * inv);
     if (part == 0) lse[(size_t)bh * N + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
@@ -182,10 +198,12 @@ bwd_dkdv_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
         const float l2 = lses[ii];
         if (!live_key || (p.causal && key > qrow) || l2 == -INFINITY) continue;
         const float pij = exp2f(s - l2);
-        const float ds = pij * (dp - Ds[ii]);
+        const float z = drop_factor(p, bh, qrow, key);
+        const float ds = pij * (dp * z - Ds[ii]);
+        const float pz = pij * z;
 #pragma unroll
         for (int t = 0; t < DS; ++t) {
-          dva[t] += pij * dos[ii][part + kTPR * t];
+          dva[t] += pz * dos[ii][part + kTPR * t];
           dka[t] += ds * qs[ii][part + kTPR * t];
         }
       }
@@ -255,7 +273,7 @@ bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
       dp = group_sum(dp);
       const int key = k0 + j;
       if (!valid_row || (p.causal && key > row) || l2 == -INFINITY) continue;
-      const float ds = exp2f(s - l2) * (dp - Di);
+      const float ds = exp2f(s - l2) * (dp * drop_factor(p, bh, row, key) - Di);
 #pragma unroll
       for (int t = 0; t < DS; ++t) acc[t] += ds * ks[j][part + kTPR * t];
     }

@@ -22,7 +22,8 @@ FA_BF16, FA_FP32 = 0, 1
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_preprocess", "fa_bwd_main",
            "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_status_string", "fa_device_error",
            "fa_selftest_wait_timeout", "fa_decode_workspace_bytes", "fa_decode",
-           "fa_fp8_vt_bytes", "fa_fp8_quantize_qk", "fa_fp8_quantize_v", "fa_fwd_fp8")
+           "fa_fp8_vt_bytes", "fa_fp8_quantize_qk", "fa_fp8_quantize_v", "fa_fwd_fp8",
+           "fa_fwd_dropout", "fa_bwd_dropout", "fa_bwd_main_dropout", "fa_dropout_random_bytes")
 
 # Largest workspace (bytes) fa_bwd_noalloc can serve from its built-in scratch array.
 FA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -79,6 +80,17 @@ def load() -> ctypes.CDLL:
     lib.fa_fp8_quantize_v.restype = I
     lib.fa_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, F, P]
     lib.fa_fwd_fp8.restype = I
+    U64, U32 = ctypes.c_ulonglong, ctypes.c_uint
+    lib.fa_fwd_dropout.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, F, I, I, U64, U32, P]
+    lib.fa_fwd_dropout.restype = I
+    lib.fa_bwd_dropout.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, F, I, I, U64,
+                                   U32, P, S, P]
+    lib.fa_bwd_dropout.restype = I
+    lib.fa_bwd_main_dropout.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, F, I, I,
+                                        U64, U32, P, S, P]
+    lib.fa_bwd_main_dropout.restype = I
+    lib.fa_dropout_random_bytes.argtypes = [P, I, I, I, U64, U32, P]
+    lib.fa_dropout_random_bytes.restype = I
     _lib = lib
     return lib
 
@@ -354,3 +366,97 @@ def attention_fp8(q, k, v, causal=False, blockmask=None, kv_len=None, scale=None
     k8, sk = fp8_quantize_qk(k, stream)
     vt8, sv = fp8_quantize_v(v, stream)
     return forward_fp8(q8, k8, vt8, sq, sk, sv, causal, blockmask, kv_len, scale, stream)
+
+
+# ----------------------------------------------------------- dropout
+
+def _drop_args(drop_threshold: int, seed: int, offset: int):
+    t = int(drop_threshold)
+    if not 0 <= t <= 255:
+        raise ValueError("drop_threshold must be in [0, 255] (drop probability t / 256)")
+    return t, int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 32 - 1)
+
+
+def fa_fwd_dropout(q, k, v, o, lse, drop_threshold: int, seed: int, offset: int = 0,
+                   causal: bool = False, blockmask=None, kv_len=None,
+                   scale: Optional[float] = None, stream=None) -> None:
+    """fa_fwd with dropout on P: element (b, h, i, j) is dropped with probability t / 256
+    (its Philox4x32-10 byte below t), kept ones are scaled by 256 / (256 - t)."""
+    _check_dense(q, k, v, o, lse, blockmask, kv_len)
+    B, H, N, d = q.shape
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    t, sd, off = _drop_args(drop_threshold, seed, offset)
+    st = load().fa_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                               int(causal), _ptr(blockmask), _ptr(kv_len), scale,
+                               _dtype_code(q), t, sd, off, _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_dropout")
+
+
+def fa_bwd_dropout(q, k, v, o, lse, do, dq, dk, dv, workspace, drop_threshold: int, seed: int,
+                   offset: int = 0, causal: bool = False, blockmask=None, kv_len=None,
+                   scale: Optional[float] = None, stream=None) -> None:
+    """Gradients of the dropped forward; the same (threshold, seed, offset) regenerate the
+    mask."""
+    _check_dense(q, k, v, o, lse, do, dq, dk, dv, blockmask, kv_len)
+    B, H, N, d = q.shape
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    t, sd, off = _drop_args(drop_threshold, seed, offset)
+    st = load().fa_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, int(causal),
+                               _ptr(blockmask), _ptr(kv_len), scale, _dtype_code(q), t, sd, off,
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_dropout")
+
+
+def fa_bwd_main_dropout(q, k, v, lse, do, dq, dk, dv, workspace, drop_threshold: int,
+                        seed: int, offset: int = 0, causal=False, blockmask=None, kv_len=None,
+                        scale=None, stream=None) -> None:
+    _check_dense(q, k, v, lse, do, dq, dk, dv, blockmask, kv_len)
+    B, H, N, d = q.shape
+    scale = 1.0 / d ** 0.5 if scale is None else float(scale)
+    t, sd, off = _drop_args(drop_threshold, seed, offset)
+    st = load().fa_bwd_main_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(do), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), B, H, N, d, int(causal),
+                                    _ptr(blockmask), _ptr(kv_len), scale, _dtype_code(q), t, sd,
+                                    off, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_main_dropout")
+
+
+def fa_dropout_random_bytes(out, seed: int, offset: int = 0, stream=None) -> None:
+    """The generator byte of every element of a [BH, n_q, n_k] uint8 tensor ``out``."""
+    if out.dtype != torch.uint8 or out.dim() != 3 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous uint8 [BH, n_q, n_k] tensor")
+    BH, n_q, n_k = out.shape
+    _, sd, off = _drop_args(0, seed, offset)
+    st = load().fa_dropout_random_bytes(_ptr(out), BH, n_q, n_k, sd, off, _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_dropout_random_bytes")
+
+
+def forward_dropout(q, k, v, drop_threshold, seed, offset=0, causal=False, blockmask=None,
+                    kv_len=None, scale=None, stream=None):
+    """Allocate O and lse with torch and run fa_fwd_dropout.  Returns (o, lse)."""
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd_dropout(q, k, v, o, lse, drop_threshold, seed, offset, causal, blockmask, kv_len,
+                   scale, stream)
+    return o, lse
+
+
+def backward_dropout(q, k, v, o, lse, do, drop_threshold, seed, offset=0, causal=False,
+                     blockmask=None, kv_len=None, scale=None, workspace=None, stream=None):
+    """Allocate dQ, dK, dV (and the workspace unless given) and run fa_bwd_dropout."""
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, N, d, q.device)
+    fa_bwd_dropout(q, k, v, o, lse, do, dq, dk, dv, workspace, drop_threshold, seed, offset,
+                   causal, blockmask, kv_len, scale, stream)
+    return dq, dk, dv

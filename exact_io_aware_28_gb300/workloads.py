@@ -39,6 +39,8 @@ class Workload:
     block_sparse: bool = False  # 128x128 block mask, diagonal kept, rest Bernoulli(p)
     keep_prob: float = 0.25
     q_head0_mult: float = 1.0   # multiply head 0 of Q (power of two: exact in bf16)
+    drop_threshold: int = 0     # dropout on P with probability drop_threshold / 256
+    drop_seed: int = 0          # the generator's 64-bit seed (an input, like the data)
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -56,6 +58,8 @@ class Workload:
             extra.append("key-padding")
         if self.block_sparse:
             extra.append(f"block-sparse p={self.keep_prob}")
+        if self.drop_threshold:
+            extra.append(f"dropout {self.drop_threshold}/256")
         return (f"{self.name}: B={self.B} H={self.H} N={self.N} d={self.d} "
                 f"{self.dtype}" + (" " + " ".join(extra) if extra else ""))
 
@@ -74,6 +78,14 @@ ORDER = ["tiny_fp32", "gpt2_causal", "bert_padded", "long_causal", "block_sparse
 
 # The FP8 forward on the long-context shape: bf16 inputs, encoded to e4m3 on the device,
 # then the e4m3 forward (same draw as long_causal).
+# Training-time attention dropout on the long-context shape: p = 26/256 (~0.1, the usual
+# attention-dropout rate), the same Q, K, V, dO draw as long_causal.
+DROPOUT_WORKLOADS = {
+    "long_causal_dropout": Workload("long_causal_dropout", 1, 32, 16384, 128, "bf16",
+                                    causal=True, drop_threshold=26,
+                                    drop_seed=0x5DEECE66D2B7E151),
+}
+
 FP8_WORKLOADS = {
     "long_causal_fp8": Workload("long_causal_fp8", 1, 32, 16384, 128, "bf16", causal=True),
 }

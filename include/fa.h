@@ -215,6 +215,55 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
                      int B, int H, int N, int d, int causal, const uint8_t* blockmask,
                      const int32_t* kv_len, float scale, void* stream);
 
+/*
+ * Attention with dropout on the probabilities.  The reading guide (arXiv 2205.14135, "Key
+ * ideas", kernel fusion) lists dropout among the steps fused into the one attention kernel;
+ * the reading taken here is inverted dropout on P:
+ *   O = (P o Z) V / (1 - p),   p = drop_threshold / 256,
+ * with lse that of the undropped softmax.  The backward regenerates Z instead of reading a
+ * stored mask and computes dV = (P o Z)^T dO / (1 - p), dS = P o (Z o dP / (1 - p) - D),
+ * D = rowsum(dO o O) of the dropped O, dQ and dK as fa_bwd.
+ *   drop_threshold : 0..255 (FA_ERR_INVALID_ARG otherwise); element (b, h, i, j) is dropped
+ *                    when its generator byte u is below it; 0 keeps everything.
+ *   seed, offset   : Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2,
+ *                    3", SC 2011) with key (seed mod 2^32, seed >> 32) and counter
+ *                    (kappa, rho, b H + h, offset), rho = 8 (i >> 4) + (i & 7),
+ *                    kappa = 4 (j >> 5) + ((j >> 1) & 3); u is byte 2 ((i >> 3) & 1) + (j & 1)
+ *                    of output word (j >> 3) & 3.  The forward and backward of one step must
+ *                    get the same (drop_threshold, seed, offset).
+ * Every other argument, layout, result and error as fa_fwd / fa_bwd / fa_bwd_main; the bf16
+ * and fp32 paths both support dropout.  fa_bwd_main_dropout is the middle stage of
+ * fa_bwd_dropout (fa_bwd_preprocess and fa_bwd_dq_convert are shared with fa_bwd).
+ */
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, int causal,
+                         const uint8_t* blockmask, const int32_t* kv_len,
+                         float scale, fa_dtype dtype, int drop_threshold,
+                         unsigned long long seed, unsigned int offset, void* stream);
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, int causal,
+                         const uint8_t* blockmask, const int32_t* kv_len,
+                         float scale, fa_dtype dtype, int drop_threshold,
+                         unsigned long long seed, unsigned int offset,
+                         void* workspace, size_t workspace_bytes, void* stream);
+fa_status fa_bwd_main_dropout(const void* q, const void* k, const void* v, const float* lse,
+                              const void* dO, void* dq, void* dk, void* dv,
+                              int B, int H, int N, int d, int causal,
+                              const uint8_t* blockmask, const int32_t* kv_len,
+                              float scale, fa_dtype dtype, int drop_threshold,
+                              unsigned long long seed, unsigned int offset,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The dropout generator's byte u(bh, i, j) of every element of a [BH, n_q, n_k] block, for
+ * inspecting a mask (dropped where u < drop_threshold).  out: device uint8 [BH, n_q, n_k],
+ * row-major; BH <= 65535, n_q * n_k <= 2^31 (FA_ERR_UNSUPPORTED otherwise).  Asynchronous on
+ * `stream`.
+ */
+fa_status fa_dropout_random_bytes(void* out, int BH, int n_q, int n_k, unsigned long long seed,
+                                  unsigned int offset, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 

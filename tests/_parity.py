@@ -7,6 +7,11 @@ where d denotes the difference between the library's output (upcast to fp64) and
 oracle's fp64 result on the same (bf16-rounded) inputs.  A gradient that is identically
 zero in exact arithmetic (N = 1 gives dQ = dK = 0) has no scale to be relative to: there
 the bound is absolute, max|grad| <= ZERO_GRAD_ABS.
+
+With dropout, O = (P o Z) V / (1 - p): the kernel's roundings of P V (P to bf16 as the MMA
+operand) and of O itself are both multiplied by the keep scale 1 / (1 - p), so the O bound
+is the plain one times that scale (``o_scale``); lse does not depend on the mask and the
+gradient bounds are already relative to max|grad|.
 """
 import numpy as np
 import torch
@@ -43,7 +48,7 @@ def run_oracle(x, heads=None):
     return o, lse, dq, dk, dv
 
 
-def compare(lib_out, ref_out, dtype, heads=None):
+def compare(lib_out, ref_out, dtype, heads=None, o_scale=1.0):
     """Assert the tolerances; returns a dict of the measured errors."""
     tol = TOL[dtype]
     o, lse, dq, dk, dv = (np64(t) for t in lib_out)
@@ -65,7 +70,7 @@ def compare(lib_out, ref_out, dtype, heads=None):
             errs[name] = float(np.abs(g).max()) / ZERO_GRAD_ABS * tol["grad"]
         else:
             errs[name] = float(np.abs(g - r).max()) / scale
-    assert errs["o"] <= tol["o"], errs
+    assert errs["o"] <= tol["o"] * max(1.0, o_scale), errs
     assert errs["lse"] <= tol["lse"], errs
     for name in ("dq", "dk", "dv"):
         assert errs[name] <= tol["grad"], (name, errs)

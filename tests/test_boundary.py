@@ -202,3 +202,67 @@ def test_fp8_encoders_reject_bad_arguments(fn, kw, code):
     f = getattr(fa.load(), fn)
     assert f(args["x"], args["x8"], args["s"], args["B"], args["H"], args["N"], args["d"],
              None) == code
+
+
+def fwd_drop(t, **kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, N=128, d=64, causal=0, bm=None,
+                kv=None, scale=0.125, dtype=fa.FA_BF16)
+    args.update(kw)
+    return fa.load().fa_fwd_dropout(args["q"], args["k"], args["v"], args["o"], args["lse"],
+                                    args["B"], args["H"], args["N"], args["d"], args["causal"],
+                                    args["bm"], args["kv"], args["scale"], args["dtype"], t,
+                                    12345, 0, None)
+
+
+def bwd_drop(t, main=False, **kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, do=A, dq=A, dk=A, dv=A, B=1, H=1, N=128, d=64,
+                causal=0, bm=None, kv=None, scale=0.125, dtype=fa.FA_BF16, ws=A,
+                wsb=1 << 30)
+    args.update(kw)
+    lib = fa.load()
+    if main:
+        return lib.fa_bwd_main_dropout(args["q"], args["k"], args["v"], args["lse"], args["do"],
+                                       args["dq"], args["dk"], args["dv"], args["B"], args["H"],
+                                       args["N"], args["d"], args["causal"], args["bm"],
+                                       args["kv"], args["scale"], args["dtype"], t, 7, 1,
+                                       args["ws"], args["wsb"], None)
+    return lib.fa_bwd_dropout(args["q"], args["k"], args["v"], args["o"], args["lse"],
+                              args["do"], args["dq"], args["dk"], args["dv"], args["B"],
+                              args["H"], args["N"], args["d"], args["causal"], args["bm"],
+                              args["kv"], args["scale"], args["dtype"], t, 7, 1, args["ws"],
+                              args["wsb"], None)
+
+
+@pytest.mark.parametrize("t", [-1, 256, 1000])
+def test_dropout_rejects_thresholds_outside_a_byte(t):
+    assert fwd_drop(t) == fa.FA_ERR_INVALID_ARG
+    assert bwd_drop(t) == fa.FA_ERR_INVALID_ARG
+    assert bwd_drop(t, main=True) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"q": None}, fa.FA_ERR_INVALID_ARG),
+    ({"d": 96}, fa.FA_ERR_UNSUPPORTED),
+    ({"scale": float("nan")}, fa.FA_ERR_INVALID_ARG),
+    ({"lse": A + 1}, fa.FA_ERR_INVALID_ARG),
+])
+def test_dropout_entry_points_validate_like_the_plain_ones(kw, code):
+    assert fwd_drop(100, **kw) == code
+    assert bwd_drop(100, **kw) == code
+
+
+def test_dropout_python_binding_checks_the_threshold():
+    with pytest.raises(ValueError):
+        fa._drop_args(256, 0, 0)
+    assert fa._drop_args(255, -1, 2 ** 32 + 5) == (255, 2 ** 64 - 1, 5)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 1, 4, 4), fa.FA_ERR_INVALID_ARG),
+    ((A, 0, 4, 4), fa.FA_ERR_INVALID_ARG),
+    ((A, 1, 0, 4), fa.FA_ERR_INVALID_ARG),
+    ((A, 70000, 4, 4), fa.FA_ERR_INVALID_ARG),
+    ((A, 1, 65536, 65536), fa.FA_ERR_UNSUPPORTED),
+])
+def test_dropout_random_bytes_rejects_bad_sizes(args, code):
+    assert fa.load().fa_dropout_random_bytes(*args, 1, 0, None) == code
