@@ -361,24 +361,41 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       if (!ok) break;
       const bool diag = p.causal && i == u.j;
       const int lim = diag ? r : 0;   // diagonal block: query column q sees key r iff q >= r
-      // Dropout: bit x of zbits keeps element (query 128 i + 64 w + x, this key row).  Query
-      // rows x and x + 8 (x % 16 < 8) share a generator call; this key's bytes sit in word
-      // (key >> 3) & 3, at byte (key & 1) for row x and 2 + (key & 1) for row x + 8.
+      // Dropout: bit x of zbits keeps element (query 128 i + 64 w + x, this key row).  Rows x
+      // and x + 8 (x % 16 < 8) share a generator call, x2 = 8 (x >> 4) + (x & 7) numbering
+      // the 32 calls of this warpgroup's columns (counter word rho = 64 i + 32 w + x2); this
+      // key's two bytes sit in word (key >> 3) & 3 at bytes (key & 1) and 2 + (key & 1).
+      // The eight lanes g = (lane & 1) + 2 ((lane >> 3) & 3) of one key octet need the same
+      // 32 calls: lane g makes calls 4g .. 4g + 3 and packs, for every partner g', the keep
+      // bits of g' (bit k + 4 s for call 4g + k, row x + 8 s) into byte g' of a 64-bit word;
+      // an 8 x 8 byte transpose over xor-shuffles hands every lane its 64 bits.
       uint64_t zbits = 0;
       if constexpr (DROP) {
-        const uint32_t octet = philox::key_octet(key), cw = (key >> 3) & 3;
-        const uint32_t sh = 8u * (key & 1);
-        const uint32_t thr = static_cast<uint32_t>(p.drop_threshold);
-#pragma unroll 4
-        for (int x2 = 0; x2 < 32; ++x2) {
-          const int x = 16 * (x2 >> 3) + (x2 & 7);
-          const philox::Words g = philox::philox4x32_10(
-              octet, philox::row_pair(i * kBlk + 64 * w + x), static_cast<uint32_t>(u.bh),
-              p.drop_offset, p.drop_seed_lo, p.drop_seed_hi);
-          const uint32_t wd = cw == 0 ? g.w[0] : cw == 1 ? g.w[1] : cw == 2 ? g.w[2] : g.w[3];
-          const uint64_t k0 = ((wd >> sh) & 0xFFu) >= thr ? 1ull : 0ull;
-          const uint64_t k1 = ((wd >> (sh + 16)) & 0xFFu) >= thr ? 1ull : 0ull;
-          zbits |= (k0 << x) | (k1 << (x + 8));
+        const uint32_t octet = philox::key_octet(key);
+        const uint32_t thr4 = 0x01010101u * static_cast<uint32_t>(p.drop_threshold);
+        const int g = (lane & 1) | (((lane >> 3) & 3) << 1);
+        uint64_t M = 0;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const philox::Words cw4 = philox::philox4x32_10(
+              octet, static_cast<uint32_t>(64 * i + 32 * w + 4 * g + kk),
+              static_cast<uint32_t>(u.bh), p.drop_offset, p.drop_seed_lo, p.drop_seed_hi);
+#pragma unroll
+          for (int cw = 0; cw < 4; ++cw) {
+            // bytes of word cw: (g' = 2cw, row x), (2cw + 1, x), (2cw, x + 8), (2cw + 1, x + 8)
+            const uint32_t t = philox::keep_bytes(cw4.w[cw], thr4) & (0x01010101u << kk);
+            const uint32_t chunk = (t & 0xFFFFu) | ((t >> 12) & 0xFFF0u);
+            M |= static_cast<uint64_t>(chunk) << (16 * cw);
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          const int src = g ^ rr;   // the partner whose calls this round's byte comes from
+          uint32_t b = static_cast<uint32_t>(M >> (8 * src)) & 0xFFu;
+          if (rr) b = __shfl_xor_sync(0xffffffffu, b, (rr & 1) | ((rr >> 1) << 3));
+          const int base = 16 * (src >> 1) + 4 * (src & 1);   // x of call 4 src, row x
+          zbits |= (static_cast<uint64_t>(b & 0xFu) << base) |
+                   (static_cast<uint64_t>(b >> 4) << (base + 8));
         }
       }
       // ---- phase A: P^T = exp2(S^T * c - lse * log2 e) for this warpgroup's 64 columns
@@ -444,6 +461,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       if (ok && n > 0) ok = mbar_wait_warp(&bars->sds_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
+      const uint64_t ks2 = f2_pack(p.drop_scale, p.drop_scale);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t dpv[32], dsp[16];
@@ -459,17 +477,19 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pp[16 * h + 2 * e4 + 1]));
           float2 d01, d23;
           if constexpr (DROP) {
-            // dS = P o (Z o dP / (1 - p) - D)
-            const int x = 32 * h + 4 * e4;
-            const float ks = p.drop_scale;
-            const float z0 = (zbits >> x) & 1 ? ks : 0.f, z1 = (zbits >> (x + 1)) & 1 ? ks : 0.f;
-            const float z2 = (zbits >> (x + 2)) & 1 ? ks : 0.f, z3 = (zbits >> (x + 3)) & 1 ? ks : 0.f;
+            // dS = P o (Z o dP / (1 - p) - D): dropped dP entries are cleared with a bit mask,
+            // the kept ones scaled by the packed keep scale.
+            const uint32_t zh = static_cast<uint32_t>(zbits >> (32 * h)) >> (4 * e4);
+            const uint32_t dp0 = dpv[4 * e4 + 0] & (0u - (zh & 1u));
+            const uint32_t dp1 = dpv[4 * e4 + 1] & (0u - ((zh >> 1) & 1u));
+            const uint32_t dp2 = dpv[4 * e4 + 2] & (0u - ((zh >> 2) & 1u));
+            const uint32_t dp3 = dpv[4 * e4 + 3] & (0u - ((zh >> 3) & 1u));
             d01 = f2_unpack(fmul2(f2_pack(p01.x, p01.y),
-                ffma2(f2_pack(__uint_as_float(dpv[4 * e4 + 0]), __uint_as_float(dpv[4 * e4 + 1])),
-                      f2_pack(z0, z1), f2_pack(nd.x, nd.y))));
+                ffma2(f2_pack(__uint_as_float(dp0), __uint_as_float(dp1)), ks2,
+                      f2_pack(nd.x, nd.y))));
             d23 = f2_unpack(fmul2(f2_pack(p23.x, p23.y),
-                ffma2(f2_pack(__uint_as_float(dpv[4 * e4 + 2]), __uint_as_float(dpv[4 * e4 + 3])),
-                      f2_pack(z2, z3), f2_pack(nd.z, nd.w))));
+                ffma2(f2_pack(__uint_as_float(dp2), __uint_as_float(dp3)), ks2,
+                      f2_pack(nd.z, nd.w))));
           } else {
             d01 = f2_unpack(fmul2(f2_pack(p01.x, p01.y),
                 fadd2(f2_pack(__uint_as_float(dpv[4 * e4 + 0]), __uint_as_float(dpv[4 * e4 + 1])), f2_pack(nd.x, nd.y))));
