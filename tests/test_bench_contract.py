@@ -54,3 +54,15 @@ def test_decode_accounting():
     # the course page's intensity: about Hq / Hkv FLOP per byte of cache
     fl, by = acc.decode_flops(32, 128, [8192]), acc.decode_bytes(32, 8, 128, [8192])
     assert fl / by == pytest.approx(32 / 8, rel=0.01)
+
+
+def test_dropout_workload_and_its_oracle_leg():
+    from exact_io_aware_28_gb300 import workloads as W
+    w = bench.TRAIN_WORKLOADS["long_causal_dropout"]
+    assert w.drop_threshold == 26 and "dropout 26/256" in w.describe()
+    assert (w.B, w.H, w.N, w.d, w.causal) == (1, 32, 16384, 128, True)
+    small = W.custom("drop_small", 1, 2, 256, 64, "bf16", causal=True, drop_threshold=26,
+                     drop_seed=5)
+    x = W.make_inputs(small, seed=0)
+    assert bench.oracle_head_seconds(x, (0, 1), small) > 0
+    assert bench.oracle_head_seconds(x, (0, 1)) > 0
