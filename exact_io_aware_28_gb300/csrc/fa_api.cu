@@ -76,7 +76,7 @@ extern "C" {
 size_t fa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lmax, int d) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || Hq % Hkv != 0) return 0;
   if (d != 64 && d != 128) return 0;
-  const size_t splits = static_cast<size_t>(decode_splits(B, Hkv, Lmax));
+  const size_t splits = static_cast<size_t>(decode_splits(B, Hkv, Lmax, d));
   return static_cast<size_t>(B) * Hq * splits * (d + 4) * sizeof(float);
 }
 
@@ -97,7 +97,7 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
   if (workspace_bytes < fa_decode_workspace_bytes(B, Hq, Hkv, Lmax, d)) return FA_ERR_INVALID_ARG;
   int* err = error_word();
   if (!err) return FA_ERR_CUDA;
-  const int splits = decode_splits(B, Hkv, Lmax);
+  const int splits = decode_splits(B, Hkv, Lmax, d);
   cudaError_t e = launch_decode(q, k, v, o, lse, B, Hq, Hkv, Lmax, d, cache_len, scale,
                                 static_cast<float*>(workspace), splits, err, wait_limit_ns(),
                                 static_cast<cudaStream_t>(stream));

@@ -398,7 +398,8 @@ cudaError_t launch_d(const void* q, const void* k, const void* v, void* o, float
 
 }  // namespace
 
-int decode_splits(int B, int Hkv, int Lmax) {
+int decode_splits(int B, int Hkv, int Lmax, int d) {
+  if (d == 128) return decode_tc_splits(B, Hkv, Lmax);
   // About eight CTAs per SM over the whole grid (two resident at a time), key ranges of at
   // least 256 keys and a whole number of 64-key tiles.
   const long long pairs = static_cast<long long>(B) * Hkv;
@@ -416,10 +417,17 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, void* o, 
                           int B, int Hq, int Hkv, int Lmax, int d, const int32_t* cache_len,
                           float scale, float* partials, int splits, int* err,
                           unsigned long long wait_ns, cudaStream_t s) {
-  return d == 64 ? launch_d<64>(q, k, v, o, lse, B, Hq, Hkv, Lmax, cache_len, scale, partials,
-                                splits, err, wait_ns, s)
-                 : launch_d<128>(q, k, v, o, lse, B, Hq, Hkv, Lmax, cache_len, scale, partials,
-                                 splits, err, wait_ns, s);
+  if (d == 64)
+    return launch_d<64>(q, k, v, o, lse, B, Hq, Hkv, Lmax, cache_len, scale, partials, splits,
+                        err, wait_ns, s);
+  // d = 128: the tensor-core split kernel (fa_decode_tc.cu), then the same combine.
+  cudaError_t e = launch_decode_tc(q, k, v, B, Hq, Hkv, Lmax, cache_len, scale, partials,
+                                   splits, err, wait_ns, s);
+  if (e != cudaSuccess) return e;
+  const int rows = B * Hq;
+  decode_combine_kernel<128><<<(rows + 7) / 8, 256, 0, s>>>(partials, B, Hq, Hkv, splits,
+                                                             static_cast<__nv_bfloat16*>(o), lse);
+  return cudaGetLastError();
 }
 
 }  // namespace fa

@@ -79,7 +79,13 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, void* o, 
                           float scale, float* partials, int splits, int* err,
                           unsigned long long wait_ns, cudaStream_t s);
 // Number of key splits per (sequence, key/value head) the decode uses on this device.
-int decode_splits(int B, int Hkv, int Lmax);
+int decode_splits(int B, int Hkv, int Lmax, int d);
+// The tensor-core split kernel for d = 128 (fa_decode_tc.cu) and its number of splits.
+int decode_tc_splits(int B, int Hkv, int Lmax);
+cudaError_t launch_decode_tc(const void* q, const void* k, const void* v, int B, int Hq,
+                             int Hkv, int Lmax, const int32_t* cache_len, float scale,
+                             float* part, int splits, int* err, unsigned long long wait_ns,
+                             cudaStream_t s);
 
 // Tensor map of a [B*H, N, d] fp32 accumulator with 32 x 32 boxes (128-byte swizzle), for bulk
 // reduce-add; rows beyond N are outside the map.
