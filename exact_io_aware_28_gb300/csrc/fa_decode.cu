@@ -19,10 +19,11 @@
 //   softmax -- one warp per query head: tile maximum and sum by shuffles, running maximum
 //              m and sum l, probabilities and the rescale factor into shared memory;
 //   P V     -- thread (pair of output columns, group of keys) accumulates all G heads.
-// The CUDA cores do this work: the step is a stream over the cache, not a contraction that
-// tensor cores would speed up.  Each split writes its unnormalised output with (m, l) to the
-// caller's fp32 workspace; the combine kernel merges the splits of each (b, h) with the same
-// rescaling rule and writes o (bf16) and lse (fp32, natural log).
+// This CUDA-core split kernel serves d = 64; for d = 128 the tensor-core split kernel of
+// fa_decode_tc.cu runs instead (on CUDA cores the fp32 conversions and about two FMAs per
+// cache byte keep the issue slots busier than HBM).  Each split writes its unnormalised
+// output with (m, l) to the caller's fp32 workspace; the combine kernel merges the splits of
+// each (b, h) with the same rescaling rule and writes o (bf16) and lse (fp32, natural log).
 #include <cuda.h>
 #include <math.h>
 
@@ -310,40 +311,64 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
 }
 
 // One warp per (b, h): merge the splits (rescale each by 2^(m_s - M)), normalise, write.
+// The split statistics are read one split per lane and the weights broadcast by shuffles;
+// each lane owns D / 32 consecutive columns and loads them as one vector per split.
 template <int D>
 __global__ void __launch_bounds__(256)
 decode_combine_kernel(const float* __restrict__ part, int B, int Hq, int Hkv, int splits,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
   constexpr int PSTRIDE = D + 4;
-  constexpr int PER = D / 32;
+  constexpr int PER = D / 32;   // 2 or 4 consecutive columns per lane
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= B * Hq) return;
   const int b = row / Hq, hq = row % Hq, G = Hq / Hkv;
   const int g = hq / G, h = hq % G;
-  const float* base = part + ((static_cast<size_t>(b) * Hkv + g) * splits) * G * PSTRIDE +
+  const size_t sstride = static_cast<size_t>(G) * PSTRIDE;   // floats between splits
+  const float* base = part + ((static_cast<size_t>(b) * Hkv + g) * splits) * sstride +
                       h * PSTRIDE;
   float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, base[static_cast<size_t>(s) * G * PSTRIDE + D]);
+  for (int s = lane; s < splits; s += 32) M = fmaxf(M, base[s * sstride + D]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   float lsum = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < splits; ++s) {
-      const float* ps = base + static_cast<size_t>(s) * G * PSTRIDE;
-      const float ms = ps[D];
-      if (ms == -INFINITY) continue;  // a split that saw no key
-      const float w = exp2f(ms - M);
-      lsum += ps[D + 1] * w;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] += ps[lane + 32 * i] * w;
+    for (int s0 = 0; s0 < splits; s0 += 32) {
+      const int s = s0 + lane;
+      float w = 0.f;
+      if (s < splits) {
+        const float ms = base[s * sstride + D];
+        w = ms == -INFINITY ? 0.f : exp2f(ms - M);   // a split that saw no key weighs 0
+        lsum += base[s * sstride + D + 1] * w;
+      }
+      const int cnt = min(32, splits - s0);
+#pragma unroll 4
+      for (int j = 0; j < cnt; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, j);
+        const float* ps = base + (s0 + j) * sstride + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(ps);
+          acc[0] += wj * v.x;
+          acc[1] += wj * v.y;
+          acc[2] += wj * v.z;
+          acc[3] += wj * v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(ps);
+          acc[0] += wj * v.x;
+          acc[1] += wj * v.y;
+        }
+      }
     }
   }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  __nv_bfloat16* orow = o + static_cast<size_t>(row) * D;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) orow[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+  for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  __nv_bfloat16* orow = o + static_cast<size_t>(row) * D + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) orow[i] = __float2bfloat16_rn(acc[i] * inv);
   if (lane == 0) lse[row] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
 }
 
