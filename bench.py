@@ -213,6 +213,16 @@ def run_reference(args, world, rank):
 
 # ------------------------------------------------------------------ GPU arm
 
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per full-size launch of ``kernel`` recorded from an ncu capture, or None."""
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(workload, {}).get(kernel)
+    except (OSError, ValueError):
+        return None
+
+
 def summarize(ms):
     """Median, p95 and the 95% Student-t interval of the mean of per-step event times (ms)."""
     ms = np.asarray(ms, dtype=np.float64)
@@ -380,14 +390,7 @@ def run_ours(args, world, rank, local):
     conv_gbs = (acc.dq_convert_bytes(B, H, N, d, elem) / (mean_phase[3] * 1e-3) / 1e9
                 if w.dtype == "bf16" else None)
     peak_t = pk["bf16_tflops_sustained"]
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            if not args.heads:
-                traffic = json.load(open(tr_path)).get(args.workload, {}).get("bwd_main")
-        except ValueError:
-            traffic = None
+    traffic = None if args.heads else recorded_traffic(args.workload, "bwd_main")
     roofline = {"kernel": "bwd main (dK, dV, dQ partials)", "bound": "tensor",
                 "achieved": main_tf, "peak": peak_t, "unit": "TFLOP/s",
                 "frac": main_tf / peak_t, "traffic": traffic,
@@ -596,7 +599,9 @@ def run_decode(args, world, rank, local):
             "timing": {"step_ms": summarize(ms)},
             "roofline": {"kernel": "decode split kernel + combine", "bound": "hbm",
                          "achieved": gbs / world, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / world / pk["hbm_gbs"], "traffic": None,
+                         "frac": gbs / world / pk["hbm_gbs"],
+                         "traffic": None if args.batch else recorded_traffic(args.workload,
+                                                                             "decode_split"),
                          "peak_kind": f"{pk['source']} HBM copy bandwidth"},
             "cpu_baseline": cpu,
             "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -778,7 +783,9 @@ def run_fp8(args, world, rank, local):
                        "hbm_peak_gbs": pk["hbm_gbs"]},
             "roofline": {"kernel": "e4m3 forward", "bound": "tensor", "achieved": fwd_tf,
                          "peak": peak8, "unit": "TFLOP/s", "frac": fwd_tf / peak8,
-                         "frac_of_burst": fwd_tf / peak8_burst, "traffic": None,
+                         "frac_of_burst": fwd_tf / peak8_burst,
+                         "traffic": None if args.heads else recorded_traffic(args.workload,
+                                                                             "fwd_fp8"),
                          "peak_kind": f"{pk['source']} bf16 dense sustained x 2 (nominal "
                                       f"fp8/bf16 ratio)"},
             "cpu_baseline": cpu,
