@@ -69,8 +69,9 @@ def test_rows_past_the_cache_length_are_never_read():
     _check(o, lse, x)
 
 
-def test_empty_cache_gives_zero_and_minus_inf():
-    w = W.DecodeWorkload("t", 3, 4, 2, 200, 64)
+@pytest.mark.parametrize("d", [64, 128])
+def test_empty_cache_gives_zero_and_minus_inf(d):
+    w = W.DecodeWorkload("t", 3, 4, 2, 200, d)
     x = W.make_decode_inputs(w, seed=6, device="cuda")
     x.cache_len = torch.tensor([0, 200, 7], dtype=torch.int32, device="cuda")
     o, lse = _run(x)
