@@ -173,14 +173,26 @@ __device__ __forceinline__ int vt_key(int k) {
   return 32 * (k >> 5) + 16 * ((k >> 2) & 1) + 8 * ((k >> 1) & 1) + 2 * ((k >> 3) & 3) + (k & 1);
 }
 
-// V, pass 2: codes of V^T with the per-head scale.  Thread task (dim, group): 16 columns
-// 16g .. 16g+15 of row `dim` of this key block, gathered from V rows vt_key(column).
+// V, pass 2: codes of V^T with the per-head scale.  The 128 x 128 block is read with
+// coalesced 16-byte loads and staged in shared memory as it lies in V ([key][dim]); thread
+// task (dim, group) then reads 16 columns 16g .. 16g+15 of row `dim` of the V^T block,
+// gathered from rows vt_key(column) (neighbouring lanes read neighbouring dims of one key:
+// no bank conflicts), and stores them as one 16-byte word.
 __global__ void __launch_bounds__(256)
 v_quant_kernel(const __nv_bfloat16* __restrict__ v, uint8_t* __restrict__ vt8,
                const unsigned* __restrict__ amax_bits, int N, int Np) {
-  const int blk = blockIdx.x, bh = blockIdx.y;
+  __shared__ __align__(16) __nv_bfloat16 sv[kBlk * kD];
+  const int blk = blockIdx.x, bh = blockIdx.y, r0 = blk * kBlk;
+  const int rows = min(kBlk, N - r0);
   const float inv = pow2f(-scale_exponent(__uint_as_float(amax_bits[bh])));
-  const __nv_bfloat16* head = v + static_cast<size_t>(bh) * N * kD;
+  {
+    uint4 x[8];
+    load_block(v + static_cast<size_t>(bh) * N * kD, r0, rows, x);   // rows past N: zero
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      reinterpret_cast<uint4*>(sv)[threadIdx.x + 256 * i] = x[i];
+  }
+  __syncthreads();
   uint8_t* out = vt8 + static_cast<size_t>(bh) * kD * Np + static_cast<size_t>(blk) * kBlk;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -190,10 +202,8 @@ v_quant_kernel(const __nv_bfloat16* __restrict__ v, uint8_t* __restrict__ vt8,
     for (int q = 0; q < 4; ++q) {
       float f[4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int key = blk * kBlk + vt_key(16 * g + 4 * q + b);
-        f[b] = key < N ? __bfloat162float(head[static_cast<size_t>(key) * kD + dim]) * inv : 0.f;
-      }
+      for (int b = 0; b < 4; ++b)
+        f[b] = __bfloat162float(sv[vt_key(16 * g + 4 * q + b) * kD + dim]) * inv;
       w[q] = e4m3x2(f[0], f[1]) | (e4m3x2(f[2], f[3]) << 16);
     }
     *reinterpret_cast<uint4*>(out + static_cast<size_t>(dim) * Np + 16 * g) =
