@@ -172,12 +172,22 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def sample_heads(time_head, H: int, min_s: float = 10.0, max_heads: int = 4):
+    """Time heads (0, 0), (0, 1), ... with ``time_head`` until about ``min_s`` seconds of CPU
+    work have run (at most ``max_heads`` heads); returns (heads timed, total seconds)."""
+    n, total = 0, 0.0
+    while n < min(H, max_heads) and (n == 0 or total < min_s):
+        total += time_head((0, n))
+        n += 1
+    return n, total
+
+
 def cpu_baseline(w: W.Workload, x_cpu) -> dict:
-    secs = oracle_head_seconds(x_cpu, (0, 0), w)
-    return {"value": head_flops(w, x_cpu) / secs / 1e12, "unit": UNIT, "cores": cpu_cores(),
+    n, secs = sample_heads(lambda hd: oracle_head_seconds(x_cpu, hd, w), w.H)
+    return {"value": n * head_flops(w, x_cpu) / secs / 1e12, "unit": UNIT, "cores": cpu_cores(),
             "kind": "oracle",
-            "sample": f"one (batch, head) of {w.describe()}: fp64 NumPy forward + backward, "
-                      f"{secs:.1f} s; FLOPs by the same convention as the GPU figure"}
+            "sample": f"{n} (batch, head) pair(s) of {w.describe()}: fp64 NumPy forward + "
+                      f"backward, {secs:.1f} s; FLOPs by the same convention as the GPU figure"}
 
 
 def run_reference(args, world, rank):
@@ -760,11 +770,11 @@ def run_fp8(args, world, rank, local):
     d2h = sum(t.numel() * t.element_size() for t in outs)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        secs = fp8_oracle_head_seconds(x_cpu, (0, 0))
-        cpu = {"value": acc.flops(1, 1, N, d, w.causal)["fwd"] / secs / 1e12, "unit": UNIT,
+        nh, secs = sample_heads(lambda hd: fp8_oracle_head_seconds(x_cpu, hd), H)
+        cpu = {"value": nh * acc.flops(1, 1, N, d, w.causal)["fwd"] / secs / 1e12, "unit": UNIT,
                "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"one (batch, head) of {w.describe()}: NumPy e4m3 encoding + fp64 "
-                         f"forward, {secs:.1f} s; FLOPs by the same convention"}
+               "sample": f"{nh} (batch, head) pair(s) of {w.describe()}: NumPy e4m3 encoding + "
+                         f"fp64 forward, {secs:.1f} s; FLOPs by the same convention"}
     if rank == 0:
         print(json.dumps({
             "metric": FP8_METRIC, "value": value, "unit": UNIT, "n_gpus": world,

@@ -66,3 +66,16 @@ def test_dropout_workload_and_its_oracle_leg():
     x = W.make_inputs(small, seed=0)
     assert bench.oracle_head_seconds(x, (0, 1), small) > 0
     assert bench.oracle_head_seconds(x, (0, 1)) > 0
+
+
+def test_cpu_sample_stops_after_the_time_budget():
+    calls = []
+
+    def fake(head):
+        calls.append(head)
+        return 4.0
+    assert bench.sample_heads(fake, H=32) == (3, 12.0)       # 4 s heads: three reach 10 s
+    assert calls == [(0, 0), (0, 1), (0, 2)]
+    assert bench.sample_heads(lambda hd: 30.0, H=32) == (1, 30.0)
+    assert bench.sample_heads(lambda hd: 0.1, H=32) == (4, 0.4)   # never more than four
+    assert bench.sample_heads(lambda hd: 0.1, H=2) == (2, 0.2)
