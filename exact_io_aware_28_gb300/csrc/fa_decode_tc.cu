@@ -1,4 +1,4 @@
-// Decode attention on the tensor cores, d = 128: the split kernel for one new query token
+// Decode attention on the tensor cores, d = 64 or 128: the split kernel for one new query token
 // per sequence over its key/value cache with grouped key/value heads (course page "Week 13.
 // GPU and FlashAttention", step 1, the bullet on attention in decode; step 2's online
 // softmax).  It writes the same per-split partials as the CUDA-core split kernel of
@@ -8,17 +8,20 @@
 // K and V; on CUDA cores that means converting every bf16 element to fp32 and about two
 // FMAs per byte, which keeps the issue slots busy before HBM is.  Here the two products run
 // as tcgen05 MMAs on tiles of 128 keys, with the G query heads padded to N = 16:
-//   S^T = K Q^T     A = K tile [128 keys][128 d] (K-major, TMA 128B swizzle),
-//                   B = Q rows of the group [16][128] (K-major)      -> TMEM, lane = key
+//   S^T = K Q^T     A = K tile [128 keys][d] (K-major, TMA 128B swizzle),
+//                   B = Q rows of the group [16][d] (K-major)        -> TMEM, lane = key
 //   O^T += V^T P^T  A = V tile read MN-major (the same TMA layout),
 //                   B = P^T [16][128 keys] bf16 (K-major)           -> TMEM, lane = d
-// and the CUDA cores only run the softmax of 128 x G scores per tile.
+// and the CUDA cores only run the softmax of 128 x G scores per tile.  The second product
+// always has M = 128: with d = 64 the second 64-row group of its A operand is a zeroed
+// shared-memory block, and the rows of O^T it produces are never read.
 //
 // Work and roles.  A unit is (sequence b, key/value head g, key range of `chunk` keys); a
 // persistent grid of at most one CTA per SM takes units blockIdx.x, + gridDim.x, ... and
 // streams their tiles through one pipeline:
 //   warp 0      TMA producer: the unit's 16 query rows (rows past the group are other heads'
-//               or zero and only feed ignored columns), then K and V tiles through 3 stages;
+//               or zero and only feed ignored columns), then K and V tiles through 3 (d =
+//               128) or 4 (d = 64) stages;
 //   warp 1      MMA issuer: S^T(n+1) is issued before O^T += V^T P^T(n) so that the scores of
 //               the next tile form while the softmax works on this one;
 //   warp 2      tensor-memory allocation (S^T x 2 [0,32), O^T x 2 [32,64));
@@ -39,22 +42,18 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kD = 128;
 constexpr int kKeys = 128;                    // keys per tile
 constexpr int kN = 16;                        // query heads padded to the MMA's N
-constexpr int kStages = 3;
+constexpr int kMaxStages = 4;
 constexpr int kSub = kKeys * 128;             // [128 rows][64 bf16] swizzled subtile, 16 KB
-constexpr int kStage = 4 * kSub;              // K tile then V tile, 64 KB
-constexpr int kQBytes = 2 * kN * 128;         // [16][128] bf16, two [16][64] subtiles
 constexpr int kPBytes = 2 * kN * 128;         // [16][128 keys] bf16
 constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kPStride = kD + 4;              // floats per (split, head) partial row
 
 struct Bars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full[2];
@@ -69,9 +68,18 @@ struct Bars {
   int never;  // stays 0: the drain wait must not be cut short by an abort
 };
 
-constexpr int kSmem = 1024 + kStages * kStage + 2 * kQBytes + 2 * kPBytes +
-                      2 * 4 * 8 * 4 * 2 + static_cast<int>(sizeof(Bars));
-static_assert(kSmem <= 227 * 1024, "shared memory");
+template <int D>
+struct TC {
+  static constexpr int NSUB = D / 64;                  // 64-column subtiles of a K or V tile
+  static constexpr int STAGES = D == 128 ? 3 : 4;
+  static constexpr int STAGE = 2 * NSUB * kSub;        // K tile then V tile
+  static constexpr int PAD = D == 128 ? 0 : kSub;      // zero rows d = 64..127 of V^T
+  static constexpr int QBYTES = NSUB * kN * 128;       // [16][d] bf16
+  static constexpr int PSTRIDE = D + 4;                // floats per (split, head) partial row
+  static constexpr int SMEM = 1024 + STAGES * STAGE + PAD + 2 * QBYTES + 2 * kPBytes +
+                              2 * 4 * 8 * 4 * 2 + static_cast<int>(sizeof(Bars));
+  static_assert(STAGES <= kMaxStages && SMEM <= 227 * 1024, "shared memory");
+};
 
 // The sequence of units and tiles every role walks in the same order.
 struct Cursor {
@@ -104,17 +112,21 @@ __device__ __forceinline__ uint32_t nk_offset(int h, int r) {
                                ((((r & 63) >> 3) ^ (h & 7)) << 4) + (r & 7) * 2);
 }
 
-template <int G>
+template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                  const __grid_constant__ CUtensorMap mq, const int32_t* __restrict__ cache_len,
                  int Hq, int Hkv, int Lmax, int splits, int chunk, int units, float c,
                  float* __restrict__ part, int* err, unsigned long long wait_ns) {
+  using C = TC<D>;
+  constexpr int kStages = C::STAGES, kStage = C::STAGE, kQBytes = C::QBYTES;
+  constexpr int kPStride = C::PSTRIDE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sKV = base;                                   // [kStages][K sub0, sub1, V sub0, sub1]
-  uint8_t* sQ = sKV + kStages * kStage;                  // [2][kQBytes]
+  uint8_t* sKV = base;                                   // [kStages][K subtiles, V subtiles]
+  uint8_t* sPad = sKV + kStages * kStage;                // d = 64: [128 keys][64] zeros
+  uint8_t* sQ = sPad + C::PAD;                           // [2][kQBytes]
   uint8_t* sP = sQ + 2 * kQBytes;                        // [2][kPBytes]
   float* red_m = reinterpret_cast<float*>(sP + 2 * kPBytes);   // [2][4 warps][8 heads]
   float* red_l = red_m + 2 * 4 * 8;                            // [2][4 warps][8 heads]
@@ -141,6 +153,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
     bars->abort = 0;
     bars->never = 0;
     fence_mbar_init();
+  }
+  if constexpr (C::PAD > 0) {
+    for (int i = tid; i < C::PAD / 16; i += kThreads)
+      reinterpret_cast<uint4*>(sPad)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();   // read by the tensor cores
   }
   if (warp == 2) {
     tmem_alloc(&bars->tmem_base, 64);
@@ -170,7 +187,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
         }
         const int b = cu.bg / Hkv, g = cu.bg % Hkv;
         mbar_arrive_expect_tx(&bars->q_full[qb], kQBytes);
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < C::NSUB; ++s)
           tma_load_3d(sQ + qb * kQBytes + s * (kN * 128), &mq, &bars->q_full[qb], 64 * s,
                       b * Hq + g * G, 0);
         for (int t = 0; t < cu.ntiles; ++t, ++n) {
@@ -182,9 +199,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
           uint8_t* dst = sKV + st * kStage;
           mbar_arrive_expect_tx(&bars->full[st], kStage);
           const int row = cu.k0 + t * kKeys;
-          for (int s = 0; s < 2; ++s) {
+          for (int s = 0; s < C::NSUB; ++s) {
             tma_load_3d(dst + s * kSub, &mk, &bars->full[st], 64 * s, row, cu.bg);
-            tma_load_3d(dst + (2 + s) * kSub, &mv, &bars->full[st], 64 * s, row, cu.bg);
+            tma_load_3d(dst + (C::NSUB + s) * kSub, &mv, &bars->full[st], 64 * s, row, cu.bg);
           }
         }
         ++nu;
@@ -229,7 +246,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
         const uint64_t dK = sw128_desc(smem_u32(sKV + st * kStage), 16, 1024);
         const uint64_t dQ = sw128_desc(smem_u32(sQ + (nu & 1) * kQBytes), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t offA = static_cast<uint64_t>(((kk >> 2) * kSub + (kk & 3) * 32) >> 4);
           const uint64_t offB = static_cast<uint64_t>(((kk >> 2) * (kN * 128) + (kk & 3) * 32) >> 4);
           mma_ss(tb + (m & 1) * kN, dK + offA, dQ + offB, idS, kk > 0 ? 1u : 0u);
@@ -253,7 +270,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
         if (!ok) break;
         tc_fence_after();
         const int st = n % kStages;
-        const uint64_t dV = sw128_desc(smem_u32(sKV + st * kStage + 2 * kSub), kSub, 1024);
+        // A = V^T, M = 128: the second group of 64 rows is the next 64 columns of V (d =
+        // 128) or the zero block (d = 64), LBO bytes further on.
+        const uint32_t aV = smem_u32(sKV + st * kStage + C::NSUB * kSub);
+        const uint32_t lbo = C::PAD > 0 ? smem_u32(sPad) - aV : static_cast<uint32_t>(kSub);
+        const uint64_t dV = sw128_desc(aV, lbo, 1024);
         const uint64_t dP = sw128_desc(smem_u32(sP + (n & 1) * kPBytes), 16, 1024);
         const uint32_t tO = tb + 32 + (nu_cur & 1) * kN;
 #pragma unroll
@@ -289,7 +310,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
       if (cu.ntiles == 0) {  // a range past the sequence's cache: an empty partial
         for (int i = r; i < G * kPStride; i += 128) {
           const int col = i % kPStride;
-          out[i] = col == kD ? -INFINITY : 0.f;
+          out[i] = col == D ? -INFINITY : 0.f;
         }
         continue;
       }
@@ -347,9 +368,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
           *reinterpret_cast<__nv_bfloat16*>(pt + nk_offset(h, r)) = __float2bfloat16_rn(p);
         }
         if (r >= valid) {  // a row past the range: zero its V so that 0 x (anything) stays 0
-          uint8_t* vt = sKV + (n % kStages) * kStage + 2 * kSub;
+          uint8_t* vt = sKV + (n % kStages) * kStage + C::NSUB * kSub;
 #pragma unroll
-          for (int s = 0; s < 2; ++s)
+          for (int s = 0; s < C::NSUB; ++s)
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
               *reinterpret_cast<uint4*>(vt + s * kSub + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
@@ -384,7 +405,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
       tmem_wait_ld();
       tc_fence_before();
 #pragma unroll
-      for (int h = 0; h < G; ++h) out[h * kPStride + r] = __uint_as_float(ov[h]);
+      if (r < D) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) out[h * kPStride + r] = __uint_as_float(ov[h]);
+      }
       float* rl = red_l + (nu & 1) * 32;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
@@ -399,8 +423,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
       if (r == 0) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          out[h * kPStride + kD] = m_run[h];
-          out[h * kPStride + kD + 1] = rl[h] + rl[8 + h] + rl[16 + h] + rl[24 + h];
+          out[h * kPStride + D] = m_run[h];
+          out[h * kPStride + D + 1] = rl[h] + rl[8 + h] + rl[16 + h] + rl[24 + h];
         }
       }
       ++nu;
@@ -422,7 +446,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
   }
 }
 
-template <int G>
+template <int D, int G>
 cudaError_t launch_g(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq,
                      const int32_t* cache_len, int Hq, int Hkv, int Lmax, int splits, int chunk,
                      int units, float c, float* part, int* err, unsigned long long wait_ns,
@@ -431,13 +455,14 @@ cudaError_t launch_g(const CUtensorMap& mk, const CUtensorMap& mv, const CUtenso
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TC<D>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int grid = units < sm_count() ? units : sm_count();
-  decode_tc_kernel<G><<<grid, kThreads, kSmem, s>>>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits,
+  decode_tc_kernel<D, G><<<grid, kThreads, TC<D>::SMEM, s>>>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits,
                                                     chunk, units, c, part, err, wait_ns);
   return cudaGetLastError();
 }
@@ -455,26 +480,40 @@ int decode_tc_splits(int B, int Hkv, int Lmax) {
   return static_cast<int>((tiles + per - 1) / per);
 }
 
-cudaError_t launch_decode_tc(const void* q, const void* k, const void* v, int B, int Hq,
-                             int Hkv, int Lmax, const int32_t* cache_len, float scale,
-                             float* part, int splits, int* err, unsigned long long wait_ns,
-                             cudaStream_t s) {
+namespace {
+
+template <int D>
+cudaError_t launch_tc_d(const void* q, const void* k, const void* v, int B, int Hq, int Hkv,
+                        int Lmax, const int32_t* cache_len, float scale, float* part, int splits,
+                        int* err, unsigned long long wait_ns, cudaStream_t s) {
   CUtensorMap mk, mv, mq;
-  if (!make_head_map_rows(&mk, k, B * Hkv, Lmax, kD, kKeys) ||
-      !make_head_map_rows(&mv, v, B * Hkv, Lmax, kD, kKeys) ||
-      !make_head_map_rows(&mq, q, 1, B * Hq, kD, kN))
+  if (!make_head_map_rows(&mk, k, B * Hkv, Lmax, D, kKeys) ||
+      !make_head_map_rows(&mv, v, B * Hkv, Lmax, D, kKeys) ||
+      !make_head_map_rows(&mq, q, 1, B * Hq, D, kN))
     return cudaErrorInvalidValue;
   const long long tiles = (Lmax + kKeys - 1) / kKeys;
   const int chunk = static_cast<int>((tiles + splits - 1) / splits) * kKeys;
   const int units = B * Hkv * splits;
   const float c = scale * kLog2e;
   switch (Hq / Hkv) {
-    case 1: return launch_g<1>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits, chunk, units, c, part, err, wait_ns, s);
-    case 2: return launch_g<2>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits, chunk, units, c, part, err, wait_ns, s);
-    case 4: return launch_g<4>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits, chunk, units, c, part, err, wait_ns, s);
-    case 8: return launch_g<8>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits, chunk, units, c, part, err, wait_ns, s);
+    case 1: return launch_g<D, 1>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits, chunk, units, c, part, err, wait_ns, s);
+    case 2: return launch_g<D, 2>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits, chunk, units, c, part, err, wait_ns, s);
+    case 4: return launch_g<D, 4>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits, chunk, units, c, part, err, wait_ns, s);
+    case 8: return launch_g<D, 8>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits, chunk, units, c, part, err, wait_ns, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const void* q, const void* k, const void* v, int B, int Hq,
+                             int Hkv, int Lmax, int d, const int32_t* cache_len, float scale,
+                             float* part, int splits, int* err, unsigned long long wait_ns,
+                             cudaStream_t s) {
+  return d == 64 ? launch_tc_d<64>(q, k, v, B, Hq, Hkv, Lmax, cache_len, scale, part, splits,
+                                   err, wait_ns, s)
+                 : launch_tc_d<128>(q, k, v, B, Hq, Hkv, Lmax, cache_len, scale, part, splits,
+                                    err, wait_ns, s);
 }
 
 }  // namespace fa

@@ -80,10 +80,10 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, void* o, 
                           unsigned long long wait_ns, cudaStream_t s);
 // Number of key splits per (sequence, key/value head) the decode uses on this device.
 int decode_splits(int B, int Hkv, int Lmax, int d);
-// The tensor-core split kernel for d = 128 (fa_decode_tc.cu) and its number of splits.
+// The tensor-core split kernel (fa_decode_tc.cu, d = 64 or 128) and its number of splits.
 int decode_tc_splits(int B, int Hkv, int Lmax);
 cudaError_t launch_decode_tc(const void* q, const void* k, const void* v, int B, int Hq,
-                             int Hkv, int Lmax, const int32_t* cache_len, float scale,
+                             int Hkv, int Lmax, int d, const int32_t* cache_len, float scale,
                              float* part, int splits, int* err, unsigned long long wait_ns,
                              cudaStream_t s);
 
