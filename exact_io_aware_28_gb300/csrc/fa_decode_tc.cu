@@ -1,8 +1,9 @@
-// Decode attention on the tensor cores, d = 64 or 128: the split kernel for one new query token
-// per sequence over its key/value cache with grouped key/value heads (course page "Week 13.
-// GPU and FlashAttention", step 1, the bullet on attention in decode; step 2's online
-// softmax).  It writes the same per-split partials as the CUDA-core split kernel of
-// fa_decode.cu, whose combine kernel merges them.
+// Decode attention on the tensor cores, d = 64 or 128: the split kernel for one new query
+// token per sequence over its key/value cache with grouped key/value heads (course page
+// "Week 13. GPU and FlashAttention", step 1, the bullet on attention in decode; step 2's
+// online softmax).  For every key range of every (sequence, key/value head) it writes the
+// unnormalised output of each query head with its running maximum and sum; the combine
+// kernel of fa_decode.cu merges the ranges.
 //
 // Why tensor cores for a stream.  Per key the step does 2 G d multiply-adds on 4 d bytes of
 // K and V; on CUDA cores that means converting every bf16 element to fp32 and about two
@@ -83,7 +84,6 @@ struct TC {
 
 // The sequence of units and tiles every role walks in the same order.
 struct Cursor {
-  int u;          // unit index (blockIdx.x + k gridDim.x)
   int bg, split;  // (sequence, key/value head) pair and key range of the unit
   int k0, k1;     // the unit's keys [k0, k1)
   int ntiles;
@@ -91,7 +91,6 @@ struct Cursor {
 
 __device__ __forceinline__ void load_unit(Cursor& c, int u, int splits, int chunk, int Hkv,
                                           int Lmax, const int32_t* cache_len) {
-  c.u = u;
   c.bg = u / splits;
   c.split = u % splits;
   const int b = c.bg / Hkv;
@@ -404,7 +403,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
       tmem_ld16(lane_base + 32 + (nu & 1) * kN, ov);
       tmem_wait_ld();
       tc_fence_before();
-#pragma unroll
       if (r < D) {
 #pragma unroll
         for (int h = 0; h < G; ++h) out[h * kPStride + r] = __uint_as_float(ov[h]);
