@@ -105,3 +105,13 @@ def test_llama8b_decode_workload_sampled():
     pairs = sorted({(int(rng.integers(w.B)), int(rng.integers(w.Hq))) for _ in range(24)})
     pairs += [(0, 0), (w.B - 1, w.Hq - 1)]
     _check(o, lse, x, pairs)
+
+
+@pytest.mark.slow
+def test_million_key_cache():
+    # A cache of 2^20 + 5 keys for one sequence (8 query heads over one K/V head, d = 128):
+    # the longest ranges and the most splits of one (sequence, head) pair, with a ragged end.
+    w = W.DecodeWorkload("t", 1, 8, 1, (1 << 20) + 5, 128)
+    x = W.make_decode_inputs(w, seed=13, device="cuda")
+    o, lse = _run(x, cache_len=False)
+    _check(o, lse, x, cache_len=False)

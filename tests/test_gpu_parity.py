@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from exact_io_aware_28_gb300 import fa
 from exact_io_aware_28_gb300 import workloads as W
 
@@ -98,3 +99,30 @@ def test_named_workload_sampled_heads(name, heads):
     # every head of the full launch is finite
     for t in out:
         assert torch.isfinite(t.float()).all() or t is out[1]
+
+
+@pytest.mark.slow
+def test_long_sequence_sampled_rows_and_gradient_sums():
+    # N = 2^16 + 77 (a ragged tail at a size far past the bench's), causal, d = 128: sampled
+    # rows of O and lse against the oracle, one row at a time; the gradients through the
+    # identities that hold at any size (rows of P sum to 1, rows of dS sum to 0):
+    #   sum_j dK_j = 0   and   sum_j dV_j = sum_i dO_i.
+    # On the GPU they are loose checks: P and dS are rounded to bf16 as MMA operands.
+    N = (1 << 16) + 77
+    x = _inputs(1, 2, N, 128, "bf16", {"causal": True}, seed=17)
+    o, lse, dq, dk, dv = run_library(x)
+    rows = np.array([0, 1, 127, 128, 4095, 32768, N - 78, N - 1])
+    q, k, v = (t.detach().to("cpu", torch.float64).numpy() for t in (x.q, x.k, x.v))
+    og, lg = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    for h in range(2):
+        keep = np.arange(N)[None, :] <= rows[:, None]
+        ro, rl, _ = oracle.forward_head(q[0, h, rows], k[0, h], v[0, h], x.scale, keep)
+        assert np.abs(og[0, h, rows] - ro).max() <= 2e-2
+        assert np.abs(lg[0, h, rows] - rl).max() <= 1e-3
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    dk64, dv64, do64 = (t.double() for t in (dk, dv, x.do))
+    sk = dk64.sum(dim=2).abs()                       # [B, H, d]
+    assert (sk <= 2e-2 * dk64.abs().sum(dim=2)).all()
+    sv, sdo = dv64.sum(dim=2), do64.sum(dim=2)
+    assert ((sv - sdo).abs() <= 2e-2 * do64.abs().sum(dim=2)).all()
