@@ -10,7 +10,12 @@ fa_bwd_main_dropout in place of fa_fwd and fa_bwd_main).  Prints ONE JSON line (
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas: the
 (batch, head) units are independent, so there is no collective on the data path); the
-timed region is bracketed by barriers and the slowest rank's time is reported.
+timed region is bracketed by barriers and the slowest rank's time is reported.  ``--gpus``
+must equal the number of ranks torchrun started (WORLD_SIZE); the script refuses otherwise.
+
+The default run (long_causal) also times the other configurations and the dropout, FP8 and
+decode workloads, each with the same CUDA events and clock sampler, and reports them in the
+line's ``per_config`` block (``--no-per-config`` skips it).
 """
 from __future__ import annotations
 
@@ -119,6 +124,16 @@ def dist_setup():
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
+
+
+def check_world(gpus: int) -> None:
+    """``--gpus N`` must match the ranks torchrun started: one process per GPU.  A mismatch
+    (for example ``--gpus 8`` without torchrun, which would time one GPU) is refused."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if gpus != world:
+        raise SystemExit(f"bench.py: --gpus {gpus} but WORLD_SIZE={world}; launch one process "
+                         f"per GPU with `python -m torch.distributed.run --nproc-per-node {gpus} "
+                         f"bench.py --gpus {gpus} ...`")
 
 
 def barrier(world):
@@ -291,26 +306,24 @@ def pipelined_e2e(steps, host_in, dev_in, dev_out, host_out, compute, comp_strea
     return t0.elapsed_time(t1) / steps
 
 
-def run_ours(args, world, rank, local):
-    from exact_io_aware_28_gb300 import fa
+def device_uuid(dev):
+    try:
+        return str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return None
 
-    dev = torch.device("cuda", torch.cuda.current_device())
-    w = TRAIN_WORKLOADS[args.workload]
-    if args.heads:
-        w = dataclasses.replace(w, H=args.heads)
-    x_cpu = W.make_inputs(w, seed=0)
-    x = W.make_inputs(w, seed=0)
-    x.q, x.k, x.v, x.do = (t.to(dev) for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.do))
-    if x.kv_len is not None:
-        x.kv_len = x.kv_len.to(dev)
-    if x.blockmask is not None:
-        x.blockmask = x.blockmask.to(dev)
+
+def measure_train(fa, w, x, steps, warmup, world, dev, tag=""):
+    """Time ``steps`` training steps (forward + the three backward stages) of workload ``w``
+    on inputs ``x`` already resident on ``dev``: CUDA events around every kernel on the
+    launching stream, nvidia-smi clocks sampled during the timed region.  Inputs smaller
+    than twice the L2 are flushed from it (a 256 MiB write) before every step."""
     B, H, N, d = w.B, w.H, w.N, w.d
     o = torch.empty_like(x.q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(x.q), torch.empty_like(x.q), torch.empty_like(x.q)
     ws = fa.alloc_workspace(B, H, N, d, dev)
-    bm_np = None if x_cpu.blockmask is None else x_cpu.blockmask.numpy()
+    bm_np = None if x.blockmask is None else x.blockmask.cpu().numpy()
     fl = acc.flops(B, H, N, d, w.causal, bm_np)
     elem = 2 if w.dtype == "bf16" else 4
     in_bytes = 4 * B * H * N * d * elem
@@ -334,6 +347,14 @@ def run_ours(args, world, rank, local):
             fa.fa_bwd_main(q_, k_, v_, lse_, do_, dq_, dk_, dv_, ws, x.causal, x.blockmask,
                            x.kv_len, x.scale, stream)
 
+    def compute(inp, out):
+        q_, k_, v_, do_ = inp
+        o_, lse_, dq_, dk_, dv_ = out
+        fwd_call(q_, k_, v_, o_, lse_)
+        fa.fa_bwd_preprocess(o_, do_, ws, stream)
+        main_call(q_, k_, v_, lse_, do_, dq_, dk_, dv_)
+        fa.fa_bwd_dq_convert(dq_, ws, x.scale, stream)
+
     def step(ev=None):
         if ev:
             ev[0].record(stream)
@@ -350,19 +371,14 @@ def run_ours(args, world, rank, local):
         if ev:
             ev[4].record(stream)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     if fa.fa_device_error() != fa.FA_OK:
-        raise RuntimeError("device error word set during warm-up")
+        raise RuntimeError(f"device error word set during warm-up {tag}")
 
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        pass
-    sampler = ClockSampler(uuid)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(device_uuid(dev))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
@@ -370,7 +386,7 @@ def run_ours(args, world, rank, local):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         if flush:
             scratch.fill_(i & 0xFF)
         step(evs[i])
@@ -379,51 +395,132 @@ def run_ours(args, world, rank, local):
     barrier(world)
     clocks = sampler.stop()
     if fa.fa_device_error() != fa.FA_OK:
-        raise RuntimeError("device error word set during the timed region")
+        raise RuntimeError(f"device error word set during the timed region {tag}")
 
     phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
-                      for i in range(args.steps)])  # ms: fwd, preprocess, main, convert
+                      for i in range(steps)])  # ms: fwd, preprocess, main, convert
     step_ms = phase.sum(axis=1)
     timing = {name: summarize(col) for name, col in
               (("step_ms", step_ms), ("fwd_ms", phase[:, 0]), ("preprocess_ms", phase[:, 1]),
                ("bwd_main_ms", phase[:, 2]), ("dq_convert_ms", phase[:, 3]))}
-    ms_per_step = float(step_ms.mean()) if flush else t_start.elapsed_time(t_end) / args.steps
+    ms_per_step = float(step_ms.mean()) if flush else t_start.elapsed_time(t_end) / steps
     ms_per_step = max_over_ranks(ms_per_step, world)
-    value = world * fl["fwd_bwd"] / (ms_per_step * 1e-3) / 1e12
-    pk = peaks()
     mean_phase = phase.mean(axis=0)
-    fwd_tf = fl["fwd"] / (mean_phase[0] * 1e-3) / 1e12
     bwd_ms = mean_phase[1:].sum()
-    bwd_tf = fl["bwd"] / (bwd_ms * 1e-3) / 1e12
-    main_tf = fl["bwd"] / (mean_phase[2] * 1e-3) / 1e12
-    pre_gbs = acc.preprocess_bytes(B, H, N, d, elem) / (mean_phase[1] * 1e-3) / 1e9
-    conv_gbs = (acc.dq_convert_bytes(B, H, N, d, elem) / (mean_phase[3] * 1e-3) / 1e9
-                if w.dtype == "bf16" else None)
-    peak_t = pk["bf16_tflops_sustained"]
+    pk = peaks()
+    value = world * fl["fwd_bwd"] / (ms_per_step * 1e-3) / 1e12
+    return {
+        "value": value, "ms_per_step": ms_per_step, "flops": fl, "flush": flush,
+        "in_bytes": in_bytes, "timing": timing, "clocks": clocks, "mean_phase": mean_phase,
+        "fwd_tflops": fl["fwd"] / (mean_phase[0] * 1e-3) / 1e12,
+        "bwd_tflops": fl["bwd"] / (bwd_ms * 1e-3) / 1e12,
+        "bwd_main_tflops": fl["bwd"] / (mean_phase[2] * 1e-3) / 1e12,
+        "preprocess_gbs": acc.preprocess_bytes(B, H, N, d, elem) / (mean_phase[1] * 1e-3) / 1e9,
+        "dq_convert_gbs": (acc.dq_convert_bytes(B, H, N, d, elem) / (mean_phase[3] * 1e-3) / 1e9
+                           if w.dtype == "bf16" else None),
+        "pct_of_peak_burst": value / world / pk["bf16_tflops"],
+        "launches": KERNELS_PER_STEP[w.dtype] * steps,
+        "compute": compute, "buffers": (o, lse, dq, dk, dv), "stream": stream,
+    }
+
+
+def device_inputs(w, dev, x_cpu=None):
+    """The workload's seeded inputs (drawn on the CPU) moved to ``dev``."""
+    x_cpu = x_cpu if x_cpu is not None else W.make_inputs(w, seed=0)
+    q, k, v, do = (t.to(dev) for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.do))
+    return W.Inputs(q, k, v, do,
+                    None if x_cpu.kv_len is None else x_cpu.kv_len.to(dev),
+                    None if x_cpu.blockmask is None else x_cpu.blockmask.to(dev),
+                    x_cpu.causal, x_cpu.scale)
+
+
+# The other configurations timed in the default run's ``per_config`` block (the headline
+# workload itself is the line's value).
+PER_CONFIG = ["tiny_fp32", "gpt2_causal", "bert_padded", "block_sparse", "long_causal_dropout",
+              "long_causal_fp8", "decode_llama8b"]
+
+
+def per_config(fa, args, world, dev, headline):
+    """Time every other configuration and workload with the same events and clock sampler
+    (at most 20 timed steps each after at least 3 warm-up steps)."""
+    steps, warmup = max(2, min(args.steps, 20)), max(3, args.warmup)
+    out = {}
+    pk = peaks()
+    for name in PER_CONFIG:
+        if name == headline:
+            continue
+        t0 = time.perf_counter()
+        if name in TRAIN_WORKLOADS:
+            w = TRAIN_WORKLOADS[name]
+            r = measure_train(fa, w, device_inputs(w, dev), steps, warmup, world, dev, name)
+            entry = {"workload": w.describe(), "metric": "fwd+bwd TFLOP/s", "value": r["value"],
+                     "fwd_tflops": r["fwd_tflops"], "bwd_tflops": r["bwd_tflops"],
+                     "bwd_main_tflops": r["bwd_main_tflops"], "ms_per_step": r["ms_per_step"],
+                     "pct_of_peak_burst": r["pct_of_peak_burst"],
+                     "timing": {"step_ms": r["timing"]["step_ms"]}, "clocks": r["clocks"],
+                     "launches": r["launches"], "steps": steps,
+                     "l2": "flushed between steps (256 MiB write)" if r["flush"] else
+                           "inputs larger than L2"}
+            if w.dtype == "fp32":
+                entry["note"] = "fp32 CUDA-core path: no tensor-core peak applies"
+                entry.pop("pct_of_peak_burst")
+        elif name in W.FP8_WORKLOADS:
+            r = measure_fp8(fa, W.FP8_WORKLOADS[name], steps, warmup, world, dev)
+            entry = {"workload": r["describe"], "metric": "fwd TFLOP/s (encode + e4m3 forward)",
+                     "value": r["value"], "fwd_kernel_tflops": r["fwd_tflops"],
+                     "ms_per_step": r["ms_per_step"],
+                     "frac_of_fp8_burst": r["fwd_tflops"] / (2.0 * pk["bf16_tflops"]),
+                     "timing": {"step_ms": r["timing"]["step_ms"]}, "clocks": r["clocks"],
+                     "launches": r["launches"], "steps": steps}
+        else:
+            r = measure_decode(fa, W.DECODE_WORKLOADS[name], steps, warmup, world, dev)
+            entry = {"workload": r["describe"], "metric": "KV-cache GB/s", "value": r["gbs"],
+                     "frac_of_hbm": r["gbs"] / world / pk["hbm_gbs"],
+                     "ms_per_step": r["ms_per_step"],
+                     "timing": {"step_ms": r["timing"]["step_ms"]}, "clocks": r["clocks"],
+                     "launches": r["launches"], "steps": steps}
+        entry["wall_s"] = time.perf_counter() - t0
+        out[name] = entry
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, world, rank, local):
+    from exact_io_aware_28_gb300 import fa
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = TRAIN_WORKLOADS[args.workload]
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads)
+    x_cpu = W.make_inputs(w, seed=0)
+    x = device_inputs(w, dev, x_cpu)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    r = measure_train(fa, w, x, args.steps, args.warmup, world, dev)
+    fl, mean_phase, value, ms_per_step = r["flops"], r["mean_phase"], r["value"], r["ms_per_step"]
+    pk = peaks()
+    main_tf = r["bwd_main_tflops"]
+    # The dominant kernel is timed by CUDA events over a sub-second region, as a kernel run
+    # in a burst: its roofline is the measured burst bf16 peak (the sustained figure, from a
+    # seconds-long loop under the power cap, is kept beside it).
+    peak_t = pk["bf16_tflops"]
     traffic = None if args.heads else recorded_traffic(args.workload, "bwd_main")
     roofline = {"kernel": "bwd main (dK, dV, dQ partials)", "bound": "tensor",
                 "achieved": main_tf, "peak": peak_t, "unit": "TFLOP/s",
                 "frac": main_tf / peak_t, "traffic": traffic,
-                "peak_kind": f"{pk['source']} bf16 dense, sustained"}
+                "peak_kind": f"{pk['source']} bf16 dense, burst",
+                "peak_sustained": pk["bf16_tflops_sustained"],
+                "frac_of_sustained": main_tf / pk["bf16_tflops_sustained"]}
 
     # e2e: the same step through the public API with every step's inputs copied from pinned
     # host memory and its results copied back, inside the timed region (pipelined).
+    o, lse, dq, dk, dv = r["buffers"]
     pin = [t.pin_memory() for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.do)]
     outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
     e2e_steps = max(2, min(args.steps, 20))
     dev_in = [(x.q, x.k, x.v, x.do), tuple(torch.empty_like(t) for t in (x.q, x.k, x.v, x.do))]
     dev_out = [(o, lse, dq, dk, dv), tuple(torch.empty_like(t) for t in (o, lse, dq, dk, dv))]
-
-    def compute(inp, out):
-        q_, k_, v_, do_ = inp
-        o_, lse_, dq_, dk_, dv_ = out
-        fwd_call(q_, k_, v_, o_, lse_)
-        fa.fa_bwd_preprocess(o_, do_, ws, stream)
-        main_call(q_, k_, v_, lse_, do_, dq_, dk_, dv_)
-        fa.fa_bwd_dq_convert(dq_, ws, x.scale, stream)
-
-    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, compute, stream),
-                            world)
+    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, r["compute"],
+                                          r["stream"]), world)
     del dev_in, dev_out
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs)
@@ -434,32 +531,37 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, x_cpu)
-
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.describe(), "B": B, "H": H, "N": N, "d": d,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed between steps (256 MiB write)" if r["flush"]
+                   else f"inputs larger than L2 ({r['in_bytes'] / 1e6:.0f} MB of Q, K, V, dO)",
+                   "flops_per_step": fl["fwd_bwd"]},
+        "pct_of_peak": value / world / peak_t,
+        "pct_of_peak_sustained": value / world / pk["bf16_tflops_sustained"],
+        "peak_kind": f"{pk['source']} bf16 dense, burst (CUDA events over a sub-second region)",
+        "timing": r["timing"],
+        "phases": {"fwd_tflops": r["fwd_tflops"], "bwd_tflops": r["bwd_tflops"],
+                   "bwd_main_tflops": main_tf,
+                   "fwd_ms": mean_phase[0], "preprocess_ms": mean_phase[1],
+                   "bwd_main_ms": mean_phase[2], "dq_convert_ms": mean_phase[3],
+                   "preprocess_gbs": r["preprocess_gbs"], "dq_convert_gbs": r["dq_convert_gbs"],
+                   "hbm_peak_gbs": pk["hbm_gbs"]},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if world == 1 and not args.no_per_config and not args.heads:
+        del x, r, o, lse, dq, dk, dv, pin, outs
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config(fa, args, world, dev, args.workload)
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": w.describe(), "B": B, "H": H, "N": N, "d": d,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "flushed between steps (256 MiB write)" if flush
-                       else f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB of Q, K, V, dO)",
-                       "flops_per_step": fl["fwd_bwd"]},
-            "pct_of_peak": value / world / peak_t,
-            "pct_of_peak_burst": value / world / pk["bf16_tflops"],
-            "timing": timing,
-            "phases": {"fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "bwd_main_tflops": main_tf,
-                       "fwd_ms": mean_phase[0], "preprocess_ms": mean_phase[1],
-                       "bwd_main_ms": mean_phase[2], "dq_convert_ms": mean_phase[3],
-                       "preprocess_gbs": pre_gbs, "dq_convert_gbs": conv_gbs,
-                       "hbm_peak_gbs": pk["hbm_gbs"]},
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": KERNELS_PER_STEP[w.dtype] * args.steps,
-            "clocks": clocks,
-        }
         print(json.dumps(line, default=float), flush=True)
 
 
@@ -511,6 +613,54 @@ def run_decode_reference(args, world, rank):
     }), flush=True)
 
 
+def measure_decode(fa, w, steps, warmup, world, dev, x_cpu=None):
+    """Time ``steps`` decode steps (split kernel + combine) of workload ``w`` with CUDA events
+    on the launching stream and the clock sampler around the timed region."""
+    x_cpu = x_cpu if x_cpu is not None else W.make_decode_inputs(w, seed=0)
+    x = W.DecodeInputs(*(t.to(dev) for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.cache_len)),
+                       w.scale)
+    stream = torch.cuda.current_stream(dev)
+    o = torch.empty_like(x.q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.L, w.d), dtype=torch.uint8,
+                     device=dev)
+
+    def compute(inp, out):
+        fa.fa_decode(inp[0], inp[1], inp[2], out[0], out[1], ws, inp[3], x.scale, stream)
+
+    for _ in range(warmup):
+        compute((x.q, x.k, x.v, x.cache_len), (o, lse))
+    torch.cuda.synchronize()
+    if fa.fa_device_error() != fa.FA_OK:
+        raise RuntimeError("device error word set during warm-up (decode)")
+    sampler = ClockSampler(device_uuid(dev))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for e0, e1 in evs:
+        e0.record(stream)
+        compute((x.q, x.k, x.v, x.cache_len), (o, lse))
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    if fa.fa_device_error() != fa.FA_OK:
+        raise RuntimeError("device error word set during the timed region (decode)")
+    ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
+    ms_per_step = max_over_ranks(float(ms.mean()), world)
+    cl = x_cpu.cache_len.numpy()
+    nbytes = acc.decode_bytes(w.Hq, w.Hkv, w.d, cl)
+    return {"describe": w.describe(), "x": x, "x_cpu": x_cpu, "o": o, "lse": lse, "ws": ws,
+            "compute": compute, "stream": stream, "ms": ms, "ms_per_step": ms_per_step,
+            "timing": {"step_ms": summarize(ms)}, "clocks": clocks, "nbytes": nbytes,
+            "gbs": world * nbytes / (ms_per_step * 1e-3) / 1e9,
+            "tflops": world * acc.decode_flops(w.Hq, w.d, cl) / (ms_per_step * 1e-3) / 1e12,
+            "launches": 2 * steps}
+
+
 def run_decode(args, world, rank, local):
     """Decode over a KV cache: fa_decode per step, KV bytes read / event time."""
     from exact_io_aware_28_gb300 import fa
@@ -522,51 +672,10 @@ def run_decode(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     fa.load()
-    x_cpu = W.make_decode_inputs(w, seed=0)
-    x = W.DecodeInputs(*(t.to(dev) for t in (x_cpu.q, x_cpu.k, x_cpu.v, x_cpu.cache_len)),
-                       w.scale)
-    stream = torch.cuda.current_stream(dev)
-    o = torch.empty_like(x.q)
-    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
-    ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.L, w.d), dtype=torch.uint8,
-                     device=dev)
-
-    def step():
-        fa.fa_decode(x.q, x.k, x.v, o, lse, ws, x.cache_len, x.scale, stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if fa.fa_device_error() != fa.FA_OK:
-        raise RuntimeError("device error word set during warm-up")
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        pass
-    sampler = ClockSampler(uuid)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.3)
-    for e0, e1 in evs:
-        e0.record(stream)
-        step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clocks = sampler.stop()
-    if fa.fa_device_error() != fa.FA_OK:
-        raise RuntimeError("device error word set during the timed region")
-    ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
-    ms_per_step = max_over_ranks(float(ms.mean()), world)
-    cl = x_cpu.cache_len.numpy()
-    nbytes = acc.decode_bytes(w.Hq, w.Hkv, w.d, cl)
-    gbs = world * nbytes / (ms_per_step * 1e-3) / 1e9
+    r = measure_decode(fa, w, args.steps, args.warmup, world, dev)
+    x, x_cpu, o, lse = r["x"], r["x_cpu"], r["o"], r["lse"]
+    gbs, nbytes, ms_per_step = r["gbs"], r["nbytes"], r["ms_per_step"]
     pk = peaks()
-    tflops = world * acc.decode_flops(w.Hq, w.d, cl) / (ms_per_step * 1e-3) / 1e12
 
     # e2e: the cache, the queries and the lengths come from pinned host memory every step and
     # o, lse go back (pipelined as for the attention step).
@@ -576,12 +685,8 @@ def run_decode(args, world, rank, local):
     dev_in = [(x.q, x.k, x.v, x.cache_len),
               tuple(torch.empty_like(t) for t in (x.q, x.k, x.v, x.cache_len))]
     dev_out = [(o, lse), (torch.empty_like(o), torch.empty_like(lse))]
-
-    def compute(inp, out):
-        fa.fa_decode(inp[0], inp[1], inp[2], out[0], out[1], ws, inp[3], x.scale, stream)
-
-    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, compute, stream),
-                            world)
+    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, r["compute"],
+                                          r["stream"]), world)
     del dev_in, dev_out
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs)
@@ -605,8 +710,8 @@ def run_decode(args, world, rank, local):
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB of KV cache)",
                        "bytes_per_step": nbytes},
-            "tflops": tflops,
-            "timing": {"step_ms": summarize(ms)},
+            "tflops": r["tflops"],
+            "timing": r["timing"],
             "roofline": {"kernel": "decode split kernel + combine", "bound": "hbm",
                          "achieved": gbs / world, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / world / pk["hbm_gbs"],
@@ -618,8 +723,8 @@ def run_decode(args, world, rank, local):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "steps": e2e_steps,
                     "copies": "pipelined: step i+1 in and step i-1 out during step i"},
-            "gpu_launches": 2 * args.steps,
-            "clocks": clocks,
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
         }, default=float), flush=True)
 
 
@@ -672,38 +777,26 @@ def run_fp8_reference(args, world, rank):
     }), flush=True)
 
 
-def run_fp8(args, world, rank, local):
-    """One step = encode Q, K, V to e4m3 (3 + 1 kernels) + the e4m3 forward (1 kernel)."""
-    from exact_io_aware_28_gb300 import fa
-    w = W.FP8_WORKLOADS[args.workload]
-    if args.heads:
-        w = dataclasses.replace(w, H=args.heads)
-    if not torch.cuda.is_available():
-        raise RuntimeError("no CUDA device: the product path has no CPU fallback")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    fa.load()
-    x_cpu = W.make_inputs(w, seed=0)
+def measure_fp8(fa, w, steps, warmup, world, dev, x_cpu=None):
+    """Time ``steps`` FP8 steps (encode Q, K, V on the device + the e4m3 forward) of workload
+    ``w`` with CUDA events on the launching stream and the clock sampler."""
+    x_cpu = x_cpu if x_cpu is not None else W.make_inputs(w, seed=0)
     q, k, v = (t.to(dev) for t in (x_cpu.q, x_cpu.k, x_cpu.v))
     B, H, N, d = w.B, w.H, w.N, w.d
     nb = (N + 127) // 128
     Np = nb * 128
     stream = torch.cuda.current_stream(dev)
-
-    def buffers():
-        return (torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
-                torch.empty((B, H, nb), dtype=torch.float32, device=dev),
-                torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
-                torch.empty((B, H, nb), dtype=torch.float32, device=dev),
-                torch.empty((B, H, d, Np), dtype=torch.uint8, device=dev),
-                torch.empty((B, H), dtype=torch.float32, device=dev))
-
-    enc = buffers()
+    enc = (torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
+           torch.empty((B, H, nb), dtype=torch.float32, device=dev),
+           torch.empty((B, H, N, d), dtype=torch.uint8, device=dev),
+           torch.empty((B, H, nb), dtype=torch.float32, device=dev),
+           torch.empty((B, H, d, Np), dtype=torch.uint8, device=dev),
+           torch.empty((B, H), dtype=torch.float32, device=dev))
     o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
 
-    def run(inp, out, e, ev=None):
-        q8, sq, k8, sk, vt8, sv = e
+    def run(inp, out, ev=None):
+        q8, sq, k8, sk, vt8, sv = enc
         if ev:
             ev[0].record(stream)
         fa.fa_fp8_quantize_qk(inp[0], q8, sq, stream)
@@ -716,42 +809,60 @@ def run_fp8(args, world, rank, local):
         if ev:
             ev[2].record(stream)
 
-    for _ in range(args.warmup):
-        run((q, k, v), (o, lse), enc)
+    for _ in range(warmup):
+        run((q, k, v), (o, lse))
     torch.cuda.synchronize()
     if fa.fa_device_error() != fa.FA_OK:
-        raise RuntimeError("device error word set during warm-up")
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        pass
-    sampler = ClockSampler(uuid)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        raise RuntimeError("device error word set during warm-up (fp8)")
+    sampler = ClockSampler(device_uuid(dev))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
-    for i in range(args.steps):
-        run((q, k, v), (o, lse), enc, evs[i])
+    for i in range(steps):
+        run((q, k, v), (o, lse), evs[i])
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
     if fa.fa_device_error() != fa.FA_OK:
-        raise RuntimeError("device error word set during the timed region")
+        raise RuntimeError("device error word set during the timed region (fp8)")
     phase = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(2)]
-                      for i in range(args.steps)])  # ms: encode, forward
+                      for i in range(steps)])  # ms: encode, forward
     step_ms = phase.sum(axis=1)
     ms_per_step = max_over_ranks(float(step_ms.mean()), world)
     fl = acc.flops(B, H, N, d, w.causal)["fwd"]
-    value = world * fl / (ms_per_step * 1e-3) / 1e12
     mean_phase = phase.mean(axis=0)
-    fwd_tf = fl / (mean_phase[1] * 1e-3) / 1e12
-    enc_gbs = acc.fp8_encode_bytes(B, H, N, d) / (mean_phase[0] * 1e-3) / 1e9
+    return {"describe": w.describe(), "x_cpu": x_cpu, "qkv": (q, k, v), "o": o, "lse": lse,
+            "run": run, "stream": stream, "flops": fl, "ms_per_step": ms_per_step,
+            "value": world * fl / (ms_per_step * 1e-3) / 1e12,
+            "fwd_tflops": fl / (mean_phase[1] * 1e-3) / 1e12,
+            "encode_gbs": acc.fp8_encode_bytes(B, H, N, d) / (mean_phase[0] * 1e-3) / 1e9,
+            "timing": {"step_ms": summarize(step_ms), "encode_ms": summarize(phase[:, 0]),
+                       "fwd_ms": summarize(phase[:, 1])},
+            "clocks": clocks, "launches": 6 * steps}
+
+
+def run_fp8(args, world, rank, local):
+    """One step = encode Q, K, V to e4m3 (3 + 1 kernels) + the e4m3 forward (1 kernel)."""
+    from exact_io_aware_28_gb300 import fa
+    w = W.FP8_WORKLOADS[args.workload]
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads)
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: the product path has no CPU fallback")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load()
+    r = measure_fp8(fa, w, args.steps, args.warmup, world, dev)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    x_cpu, (q, k, v), o, lse = r["x_cpu"], r["qkv"], r["o"], r["lse"]
+    fl, value, ms_per_step, fwd_tf = r["flops"], r["value"], r["ms_per_step"], r["fwd_tflops"]
     pk = peaks()
-    # Dense fp8 peak: the measured bf16 figure times the nominal fp8 / bf16 ratio (4.5 / 2.25).
-    peak8 = 2.0 * pk["bf16_tflops_sustained"]
-    peak8_burst = 2.0 * pk["bf16_tflops"]
+    # Dense fp8 peak: the measured burst bf16 figure times the nominal fp8 / bf16 ratio
+    # (4.5 / 2.25); the forward kernel is timed by CUDA events over a sub-second region.
+    peak8 = 2.0 * pk["bf16_tflops"]
+    peak8_sustained = 2.0 * pk["bf16_tflops_sustained"]
 
     pin = [t.pin_memory() for t in (x_cpu.q, x_cpu.k, x_cpu.v)]
     outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
@@ -761,10 +872,10 @@ def run_fp8(args, world, rank, local):
 
     def compute(inp, out):
         # the codes live on the compute stream only: one set serves every step
-        run(inp, out, enc)
+        r["run"](inp, out)
 
-    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, compute, stream),
-                            world)
+    e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, compute,
+                                          r["stream"]), world)
     del dev_in, dev_out
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs)
@@ -787,24 +898,23 @@ def run_fp8(args, world, rank, local):
                        "l2": "inputs larger than L2 (402 MB of bf16 Q, K, V at the full size)",
                        "flops_per_step": fl},
             "pct_of_peak": value / world / peak8,
-            "timing": {"step_ms": summarize(step_ms), "encode_ms": summarize(phase[:, 0]),
-                       "fwd_ms": summarize(phase[:, 1])},
-            "phases": {"encode_gbs": enc_gbs, "fwd_kernel_tflops": fwd_tf,
+            "timing": r["timing"],
+            "phases": {"encode_gbs": r["encode_gbs"], "fwd_kernel_tflops": fwd_tf,
                        "hbm_peak_gbs": pk["hbm_gbs"]},
             "roofline": {"kernel": "e4m3 forward", "bound": "tensor", "achieved": fwd_tf,
                          "peak": peak8, "unit": "TFLOP/s", "frac": fwd_tf / peak8,
-                         "frac_of_burst": fwd_tf / peak8_burst,
+                         "frac_of_sustained": fwd_tf / peak8_sustained,
                          "traffic": None if args.heads else recorded_traffic(args.workload,
                                                                              "fwd_fp8"),
-                         "peak_kind": f"{pk['source']} bf16 dense sustained x 2 (nominal "
+                         "peak_kind": f"{pk['source']} bf16 dense burst x 2 (nominal "
                                       f"fp8/bf16 ratio)"},
             "cpu_baseline": cpu,
             "e2e": {"value": world * fl / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "steps": e2e_steps,
                     "copies": "pipelined: step i+1 in and step i-1 out during step i"},
-            "gpu_launches": 6 * args.steps,
-            "clocks": clocks,
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
         }, default=float), flush=True)
 
 
@@ -819,6 +929,8 @@ def main():
                     list(W.FP8_WORKLOADS),
                     default="long_causal")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config block of the default run")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the workload's head count (smaller cases for profiling)")
     ap.add_argument("--batch", type=int, default=0,
@@ -826,6 +938,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    check_world(args.gpus)
     world, rank, local = dist_setup()
     decode = args.workload in W.DECODE_WORKLOADS
     fp8 = args.workload in W.FP8_WORKLOADS

@@ -79,3 +79,31 @@ def test_cpu_sample_stops_after_the_time_budget():
     assert bench.sample_heads(lambda hd: 30.0, H=32) == (1, 30.0)
     assert bench.sample_heads(lambda hd: 0.1, H=32) == (4, 0.4)   # never more than four
     assert bench.sample_heads(lambda hd: 0.1, H=2) == (2, 0.2)
+
+
+def test_gpus_must_match_the_ranks_started(monkeypatch):
+    # --gpus 8 without torchrun would time one GPU and call it eight: refused up front.
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    bench.check_world(1)
+    with pytest.raises(SystemExit, match="WORLD_SIZE=1"):
+        bench.check_world(8)
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.check_world(2)
+    with pytest.raises(SystemExit):
+        bench.check_world(1)
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "4",
+                          "--impl", "reference", "--workload", "tiny_fp32"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT,
+                         env={k: v for k, v in os.environ.items() if k != "WORLD_SIZE"})
+    assert out.returncode != 0 and "WORLD_SIZE=1" in out.stderr
+    assert not [l for l in out.stdout.splitlines() if l.startswith("{")]
+
+
+def test_per_config_covers_every_other_workload():
+    from exact_io_aware_28_gb300 import workloads as W
+    names = set(bench.PER_CONFIG)
+    # the four other scope configurations, the dropout and FP8 steps and decode
+    assert set(W.ORDER) - {"long_causal"} <= names
+    assert {"long_causal_dropout", "long_causal_fp8", "decode_llama8b"} <= names
+    for n in names:
+        assert n in bench.TRAIN_WORKLOADS or n in W.FP8_WORKLOADS or n in W.DECODE_WORKLOADS

@@ -212,6 +212,45 @@ def test_batched_wrappers_match_heads():
     assert np.isnan(sub_o[0, 0]).all() and np.isfinite(sub_o[1, 2]).all()
 
 
+def test_block_mask_indexing_explicit_matrix():
+    # A 4 x 4 block mask over 2 x 2 blocks, written out element by element: the mask entry
+    # [row block, column block] decides the query-row x key-column square it covers (a
+    # transposed or shifted lookup fails here).
+    bm = np.array([[1, 0, 0, 1],
+                   [0, 1, 1, 0],
+                   [1, 1, 0, 0],
+                   [0, 0, 1, 1]], dtype=np.uint8)
+    expected = np.array([
+        [1, 1, 0, 0, 0, 0, 1, 1],
+        [1, 1, 0, 0, 0, 0, 1, 1],
+        [0, 0, 1, 1, 1, 1, 0, 0],
+        [0, 0, 1, 1, 1, 1, 0, 0],
+        [1, 1, 1, 1, 0, 0, 0, 0],
+        [1, 1, 1, 1, 0, 0, 0, 0],
+        [0, 0, 0, 0, 1, 1, 1, 1],
+        [0, 0, 0, 0, 1, 1, 1, 1]], dtype=bool)
+    np.testing.assert_array_equal(A.keep_mask(8, blockmask=bm, block=2), expected)
+    # Ragged last block (n = 7): the last row and column of the mask cover one element.
+    np.testing.assert_array_equal(A.keep_mask(7, blockmask=bm, block=2), expected[:7, :7])
+    # Combined with the causal mask and a key length: the intersection, element by element.
+    both = A.keep_mask(8, causal=True, blockmask=bm, kv_len=5, block=2)
+    expected_both = np.array([
+        [1, 0, 0, 0, 0, 0, 0, 0],
+        [1, 1, 0, 0, 0, 0, 0, 0],
+        [0, 0, 1, 0, 0, 0, 0, 0],
+        [0, 0, 1, 1, 0, 0, 0, 0],
+        [1, 1, 1, 1, 0, 0, 0, 0],
+        [1, 1, 1, 1, 0, 0, 0, 0],
+        [0, 0, 0, 0, 1, 0, 0, 0],
+        [0, 0, 0, 0, 1, 0, 0, 0]], dtype=bool)
+    np.testing.assert_array_equal(both, expected_both)
+    # The default block is the pages' 128 x 128: one mask entry covers 128 x 128 pairs.
+    bm2 = np.array([[1, 0], [1, 1]], dtype=np.uint8)
+    keep = A.keep_mask(200, blockmask=bm2)
+    assert keep[:128, :128].all() and not keep[:128, 128:].any()
+    assert keep[128:, :].all()
+
+
 # -------------------------------------------- independent online-softmax reference
 
 @pytest.mark.parametrize("br,bc", [(1, 1), (16, 32), (128, 128), (None, None)])

@@ -15,7 +15,7 @@ import torch
 from exact_io_aware_28_gb300 import fa
 from exact_io_aware_28_gb300 import workloads as W
 
-from _parity import TOL
+from _parity import TOL, compare, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -71,6 +71,18 @@ def test_fp32_and_masks_match_fa_bwd():
     ref = fa.backward(x.q, x.k, x.v, o, lse, x.do, False, x.blockmask, None, x.scale)
     for _ in range(2):
         _close(_noalloc(x, o, lse), ref, "bf16")
+
+
+def test_matches_the_oracle_directly():
+    # The same check against the CPU fp64 oracle rather than against fa_bwd: causal, two
+    # calls in a row, every gradient within the bf16 tolerances.
+    w = W.custom("noalloc_oracle", 1, 2, 384, 128, "bf16", causal=True)
+    x = W.make_inputs(w, seed=25, device="cuda")
+    o, lse = fa.forward(x.q, x.k, x.v, x.causal, None, None, x.scale)
+    ref = run_oracle(x)
+    for _ in range(2):
+        dq, dk, dv = _noalloc(x, o, lse)
+        compare((o, lse, dq, dk, dv), ref, "bf16")
 
 
 def test_rejects_problems_larger_than_the_scratch_array():
