@@ -5,14 +5,18 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <atomic>
+
 #include "fa_internal.cuh"
 
 namespace fa {
 
 namespace {
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices];      // 0 = not yet queried
-int* g_err_ptr[kMaxDevices];      // device address of the error word, per device
+// Per-device caches.  Host threads may fill them concurrently: each slot is atomic and a
+// race only stores the same value twice.
+std::atomic<int> g_sm_count[kMaxDevices];    // 0 = not yet queried
+std::atomic<int*> g_err_ptr[kMaxDevices];    // device address of the error word
 }  // namespace
 
 // Device error word: a kernel whose bounded wait runs out stores FA_ERR_TIMEOUT here.
@@ -22,24 +26,26 @@ int sm_count() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= kMaxDevices) return 148;
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
+  int n = g_sm_count[dev].load();
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
-    g_sm_count[dev] = n;
+    g_sm_count[dev].store(n);
   }
-  return g_sm_count[dev];
+  return n;
 }
 
 int* error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_err_ptr[dev]) {
+  int* cached = g_err_ptr[dev].load();
+  if (!cached) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<int*>(ptr);
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess || !ptr) return nullptr;
+    cached = static_cast<int*>(ptr);
+    g_err_ptr[dev].store(cached);
   }
-  return g_err_ptr[dev];
+  return cached;
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
@@ -55,15 +61,15 @@ fa_status check_shape(int B, int H, int N, int d) {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 unsigned long long wait_limit_ns() {
-  static unsigned long long ns = 0;
-  if (ns == 0) {
+  // Initialised once (a function-local static is thread-safe).
+  static const unsigned long long ns = [] {
     unsigned long long v = 2000ull;
     if (const char* s = getenv("FA_WAIT_LIMIT_MS")) {
       const long long ms = atoll(s);
       if (ms > 0 && ms < 600000) v = static_cast<unsigned long long>(ms);
     }
-    ns = v * 1000000ull;
-  }
+    return v * 1000000ull;
+  }();
   return ns;
 }
 

@@ -32,6 +32,8 @@
 //               zeroed in the V tile before the product reads it; O^T is rescaled in TMEM
 //               only when a head's maximum grows by more than 2^8.
 // Every wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and leaves.
+#include <atomic>
+
 #include <cuda.h>
 #include <math.h>
 
@@ -449,15 +451,15 @@ cudaError_t launch_g(const CUtensorMap& mk, const CUtensorMap& mv, const CUtenso
                      const int32_t* cache_len, int Hq, int Hkv, int Lmax, int splits, int chunk,
                      int units, float c, float* part, int* err, unsigned long long wait_ns,
                      cudaStream_t s) {
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device; a race repeats the same call
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<D, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TC<D>::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true);
   }
   const int grid = units < sm_count() ? units : sm_count();
   decode_tc_kernel<D, G><<<grid, kThreads, TC<D>::SMEM, s>>>(mk, mv, mq, cache_len, Hq, Hkv, Lmax, splits,

@@ -37,6 +37,8 @@
 //               in shared memory and stored with the TMA; logsumexp per row.
 // O is rescaled only when a row's maximum grows by more than 2^8, so P <= 256 < 448 always
 // fits e4m3.  Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT.
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_fp8.h>
 #include <math.h>
@@ -604,14 +606,14 @@ cudaError_t launch_fwd_fp8(const Problem& p, const void* q8, const void* k8, con
   if (!make_u8_map(&mq, q8, BH, p.N, kD) || !make_u8_map(&mk, k8, BH, p.N, kD) ||
       !make_u8_map(&mvt, vt8, BH, kD, Np) || !make_head_map(&mo, o, BH, p.N, kD))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device; a race repeats the same call
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load()) {
     cudaError_t e =
         cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true);
   }
   const int nqb = (p.N + 2 * kBlk - 1) / (2 * kBlk);
   fwd_fp8_kernel<<<dim3(static_cast<unsigned>(BH) * nqb), kThreads, kSmem, s>>>(

@@ -25,6 +25,8 @@
 //   epilogue      the softmax warps read O from TMEM, divide by the row sum and store bf16.
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [384,384+d).
 // Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and exits cleanly.
+#include <atomic>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -449,15 +451,16 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  // Looked up once (a function-local static is thread-safe); null if the driver lacks it.
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -522,14 +525,14 @@ static cudaError_t fwd_launch(const Problem& p, const void* q, const void* k, co
   if (!make_head_map(&mq, q, BH, p.N, D) || !make_head_map(&mk, k, BH, p.N, D) ||
       !make_head_map(&mv, v, BH, p.N, D) || !make_head_map(&mo, o, BH, p.N, D))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device; a race repeats the same call
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<D, DROP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true);
   }
   const int nqb = (p.N + 255) / 256;
   dim3 grid(static_cast<unsigned>(BH) * nqb);

@@ -27,6 +27,8 @@ struct Problem {
   int drop_threshold = 0;
   uint32_t drop_seed_lo = 0, drop_seed_hi = 0, drop_offset = 0;
   float drop_scale = 1.f;    // 256 / (256 - drop_threshold)
+  // Backward launch order: heads per group of CTAs (set by the backward launcher).
+  int head_group = 1;
 };
 
 // Bound of device-side waits: FA_WAIT_LIMIT_MS from the environment (read once), else 2 s.
@@ -86,6 +88,13 @@ cudaError_t launch_decode_tc(const void* q, const void* k, const void* v, int B,
                              int Hkv, int Lmax, int d, const int32_t* cache_len, float scale,
                              float* part, int splits, int* err, unsigned long long wait_ns,
                              cudaStream_t s);
+
+// Sequence sharding (fa_shard.cu): merge of partial (O, lse) results, fp32 gradient sums.
+cudaError_t launch_merge(const void* o_parts, const float* lse_parts, int S, void* o, float* lse,
+                         long long rows, int d, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_accumulate(float* acc, const void* x, long long n, fa_dtype dt,
+                              cudaStream_t s);
+cudaError_t launch_finish(void* out, const float* acc, long long n, fa_dtype dt, cudaStream_t s);
 
 // Tensor map of a [B*H, N, d] fp32 accumulator with 32 x 32 boxes (128-byte swizzle), for bulk
 // reduce-add; rows beyond N are outside the map.

@@ -12,11 +12,15 @@
 // FA_NOALLOC_SCRATCH_BYTES of it until the process exits.  In host code its name only
 // stands in for the symbol, it is not a device address, so the address is fetched with
 // cudaGetSymbolAddress, once per device, with that device current, on the first call
-// made on that device (make that first call before any stream capture).  All calls share
+// made on that device (make that first call before any stream capture).  That first call
+// is safe from several host threads at once: the cached address is atomic and each thread
+// that races stores the same value.  All calls share
 // the one array and it keeps the previous call's contents: the preprocess stage rewrites
 // D and zeroes the accumulator at the start of every call, and two calls whose work
 // overlaps on the GPU (for example on two streams) race on it.
 #include <stdint.h>
+
+#include <atomic>
 
 #include "fa_internal.cuh"
 
@@ -26,18 +30,20 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices];  // device address of the array, per device
+std::atomic<void*> g_scratch_ptr[kMaxDevices];  // device address of the array, per device
 
 // Device address of the scratch array on the current device, or nullptr on failure.
 void* scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_scratch_ptr[dev]) {
+  void* cached = g_scratch_ptr[dev].load();
+  if (!cached) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
-    g_scratch_ptr[dev] = ptr;
+    g_scratch_ptr[dev].store(ptr);
+    cached = ptr;
   }
-  return g_scratch_ptr[dev];
+  return cached;
 }
 
 }  // namespace

@@ -23,7 +23,11 @@ EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_preprocess", "f
            "fa_bwd_dq_convert", "fa_bwd_noalloc", "fa_status_string", "fa_device_error",
            "fa_selftest_wait_timeout", "fa_decode_workspace_bytes", "fa_decode",
            "fa_fp8_vt_bytes", "fa_fp8_quantize_qk", "fa_fp8_quantize_v", "fa_fwd_fp8",
-           "fa_fwd_dropout", "fa_bwd_dropout", "fa_bwd_main_dropout", "fa_dropout_random_bytes")
+           "fa_fwd_dropout", "fa_bwd_dropout", "fa_bwd_main_dropout", "fa_dropout_random_bytes",
+           "fa_attn_merge", "fa_grad_accumulate", "fa_grad_finish")
+
+# Largest number of partial results fa_attn_merge accepts.
+FA_MERGE_MAX_PARTS = 1024
 
 # Largest workspace (bytes) fa_bwd_noalloc can serve from its built-in scratch array.
 FA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -91,6 +95,13 @@ def load() -> ctypes.CDLL:
     lib.fa_bwd_main_dropout.restype = I
     lib.fa_dropout_random_bytes.argtypes = [P, I, I, I, U64, U32, P]
     lib.fa_dropout_random_bytes.restype = I
+    L = ctypes.c_longlong
+    lib.fa_attn_merge.argtypes = [P, P, I, P, P, I, I, I, I, I, P]
+    lib.fa_attn_merge.restype = I
+    lib.fa_grad_accumulate.argtypes = [P, P, L, I, P]
+    lib.fa_grad_accumulate.restype = I
+    lib.fa_grad_finish.argtypes = [P, P, L, I, P]
+    lib.fa_grad_finish.restype = I
     _lib = lib
     return lib
 
@@ -460,3 +471,42 @@ def backward_dropout(q, k, v, o, lse, do, drop_threshold, seed, offset=0, causal
     fa_bwd_dropout(q, k, v, o, lse, do, dq, dk, dv, workspace, drop_threshold, seed, offset,
                    causal, blockmask, kv_len, scale, stream)
     return dq, dk, dv
+
+
+# ----------------------------------------------------------- sequence sharding
+
+def fa_attn_merge(o_parts, lse_parts, o, lse, stream=None) -> None:
+    """Merge S partial (O, lse) results of the same rows over disjoint key sets:
+    o_parts [S, B, H, N, d], lse_parts fp32 [S, B, H, N] -> o [B, H, N, d], lse [B, H, N]."""
+    _check_dense(o_parts, lse_parts, o, lse)
+    S, B, H, N, d = o_parts.shape
+    if tuple(lse_parts.shape) != (S, B, H, N) or lse_parts.dtype != torch.float32:
+        raise ValueError("lse_parts must be fp32 [S, B, H, N]")
+    if o.dtype != o_parts.dtype:
+        raise TypeError("o and o_parts must have the same dtype")
+    st = load().fa_attn_merge(_ptr(o_parts), _ptr(lse_parts), S, _ptr(o), _ptr(lse), B, H, N, d,
+                              _dtype_code(o_parts), _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_attn_merge")
+
+
+def fa_grad_accumulate(acc, x, stream=None) -> None:
+    """acc (fp32) += x (bf16 or fp32, same number of elements)."""
+    _check_dense(acc, x)
+    if acc.dtype != torch.float32 or acc.numel() != x.numel():
+        raise ValueError("acc must be fp32 with as many elements as x")
+    st = load().fa_grad_accumulate(_ptr(acc), _ptr(x), acc.numel(), _dtype_code(x),
+                                   _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_grad_accumulate")
+
+
+def fa_grad_finish(out, acc, stream=None) -> None:
+    """out (bf16 or fp32) = acc (fp32) rounded once."""
+    _check_dense(acc, out)
+    if acc.dtype != torch.float32 or acc.numel() != out.numel():
+        raise ValueError("acc must be fp32 with as many elements as out")
+    st = load().fa_grad_finish(_ptr(out), _ptr(acc), acc.numel(), _dtype_code(out),
+                               _stream(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_grad_finish")

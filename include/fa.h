@@ -264,6 +264,54 @@ fa_status fa_bwd_main_dropout(const void* q, const void* k, const void* v, const
 fa_status fa_dropout_random_bytes(void* out, int BH, int n_q, int n_k, unsigned long long seed,
                                   unsigned int offset, void* stream);
 
+/*
+ * Attention split over key/value shards of one sequence (sequence sharding).
+ *
+ * The FlashAttention reading guide (arXiv 2205.14135) merges the softmax statistics of a
+ * vector split into parts ("Method": m = max(m1, m2), l = e^{m1 - m} l1 + e^{m2 - m} l2)
+ * and names attention over several GPUs as open work ("Limitations").  When the keys and
+ * values of a sequence are split into S shards, fa_fwd on (the queries, one shard) gives a
+ * partial (O_k, lse_k) normalised over that shard's keys; fa_attn_merge combines them:
+ *   lse = ln sum_k e^{lse_k},   O = sum_k e^{lse_k - lse} O_k,
+ * which is the attention over all the keys.  For the backward, fa_bwd_preprocess of the
+ * merged (O, dO) gives D and zeroes the dQ accumulator; fa_bwd_main with the merged lse
+ * then runs once per shard, adding each shard's dQ contribution to the same accumulator and
+ * writing that shard's dK, dV contributions; fa_grad_accumulate sums contributions to a
+ * shard's dK, dV that come from several query shards, fa_grad_finish rounds a sum to the
+ * output type, and fa_bwd_dq_convert finishes dQ.
+ */
+
+/* Largest number of partial results fa_attn_merge accepts. */
+#define FA_MERGE_MAX_PARTS 1024
+
+/*
+ * Merge S partial results of the same query rows over disjoint key sets.
+ *   o_parts  in : [S, B, H, N, d] of `dtype` (part k at o_parts + k * B*H*N*d), each part
+ *                 normalised over its own keys (a fa_fwd output); 16-byte aligned.
+ *   lse_parts in: fp32 [S, B, H, N], the parts' logsumexps; -inf where a part has no
+ *                 visible key (that part then weighs nothing).
+ *   o        out: [B, H, N, d] of `dtype`; 0 in a row that no part sees.
+ *   lse      out: fp32 [B, H, N]; -inf in a row that no part sees.
+ *   S             1 .. FA_MERGE_MAX_PARTS.  d = 64 or 128.  o must not alias o_parts.
+ * Returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED before launching on a bad argument.
+ */
+fa_status fa_attn_merge(const void* o_parts, const float* lse_parts, int S, void* o, float* lse,
+                        int B, int H, int N, int d, fa_dtype dtype, void* stream);
+
+/*
+ * acc[i] += x[i] for i < n: fp32 running sum of gradient contributions (for example the dK of
+ * one key shard from several query shards).  acc: device fp32, 16-byte aligned; x: device,
+ * `dtype` elements, 8-byte (bf16) or 16-byte (fp32) aligned; n a positive multiple of 4.
+ */
+fa_status fa_grad_accumulate(float* acc, const void* x, long long n, fa_dtype dtype,
+                             void* stream);
+
+/*
+ * out[i] = acc[i] rounded once (round-to-nearest-even) to `dtype`, for i < n.  Alignment and
+ * n as for fa_grad_accumulate.
+ */
+fa_status fa_grad_finish(void* out, const float* acc, long long n, fa_dtype dtype, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa_status_string(fa_status s);
 
