@@ -16,25 +16,33 @@
 // the causal mask, mask[i][j] = 1 under a block mask), accumulating dK_j, dV_j in tensor
 // memory and adding each dQ_i partial to an fp32 accumulator in global memory.
 // Per query block the tensor pipe runs five MMAs (all M = 128, bf16 in, fp32 out):
-//   S^T  = K_j Q_i^T   (A: K_j K-major smem,    B: Q_i K-major smem)    -> TMEM [0,128)
-//   dP^T = V_j dO_i^T  (A: V_j K-major smem,    B: dO_i K-major smem)   -> TMEM [128,256)
+//   S^T  = K_j Q_i^T   (A: K_j K-major smem,    B: Q_i K-major smem)    -> TMEM R0
+//   dP^T = V_j dO_i^T  (A: V_j K-major smem,    B: dO_i K-major smem)   -> TMEM R1
 //   dV  += P^T dO_i    (A: P^T bf16 in TMEM,    B: dO_i MN-major smem)  -> TMEM [256,256+d)
-//   dK  += dS^T Q_i    (A: dS^T bf16 in TMEM,   B: Q_i MN-major smem)   -> TMEM [384,384+d)
-//   dQ_i = dS K_j      (A: dS^T MN-major smem,  B: K_j MN-major smem)   -> TMEM [0,d)
-// P^T is written over already-read S^T columns and dS^T over already-read dP^T columns;
-// dQ_i (TMEM lane = query row) goes into the S^T region once dV has read P^T.
+//   dK  += dS^T Q_i    (A: dS^T bf16 in TMEM,   B: Q_i MN-major smem)   -> TMEM dK columns
+//   dQ_i = dS K_j      (A: dS^T MN-major smem,  B: K_j MN-major smem)   -> TMEM dQ columns
+// with R0 = [0,128) and R1 = [128,256).  P^T is written over already-read S^T columns and
+// dS^T over already-read dP^T columns.  With d = 128 the dQ partial (TMEM lane = query row)
+// goes into R0 once dV has read P^T there (dK at [384,512)); with d = 64 it has columns of its
+// own, [320,384) (dK at [384,448)).
 // Warps (16): 0-3 the dQ drain, 4-7 and 8-11 two warpgroups that each take 64 of the 128
 // query columns of every key row (phase A: P^T from S^T; phase B: dS^T from dP^T), 12 TMA
 // producer (K_j, V_j once; Q_i and dO_i through two-stage rings) and tensor-memory
 // allocation, 13 MMA issuer, 14-15 idle.  The drain copies each dQ_i partial out of TMEM
 // into 128-byte-swizzled [32 rows][32 columns] fp32 boxes in shared memory and adds them to
 // the fp32 accumulator in global memory with TMA bulk reduce-adds.
-// MMA issue order per block n: dV(n), dQ(n), S^T(n+1), dK(n), dP^T(n+1).  The dQ drain
-// and the bulk reduce-adds behind it decide when the next phase B may reuse the dS tile,
-// so dQ(n) goes first once phase B(n) is done; the drain copies the whole partial out of
-// TMEM in one load, and S^T(n+1) follows as soon as it has, so the next phase A starts
+// MMA issue order per block n, d = 128: dV(n), dQ(n), S^T(n+1), dK(n), dP^T(n+1).  The dQ
+// drain and the bulk reduce-adds behind it decide when the next phase B may reuse the dS
+// tile, so dQ(n) goes first once phase B(n) is done; the drain copies the whole partial out
+// of TMEM in one load, and S^T(n+1) follows as soon as it has, so the next phase A starts
 // early; dP^T(n+1) needs only dK(n) to have read dS^T(n).
+// d = 64: dV(n), S^T(n+1), then (after phase B(n)) dQ(n), dK(n), dP^T(n+1): with dQ in columns
+// of its own nothing waits for the drain, and S^T(n+1) goes into R0 as soon as dV(n) (issued
+// before it; one thread's MMAs run in issue order) has read P^T(n), so it is ready when the
+// softmax warps finish phase B(n).
 // Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and exits.
+#include <atomic>
+
 #include <cuda.h>
 #include <math.h>
 
@@ -65,6 +73,11 @@ struct Cfg {
   static constexpr int NSTAGE = 2;                 // Q_i / dO_i ring
   static constexpr int DS = 2 * kSub;              // dS^T, 128 x 128 bf16
   static constexpr int SMEM = 1024 + 2 * TILE + NSTAGE * 2 * TILE + DS + 1024 + 256;
+  // TMEM columns of the dQ partial: R0 (after dV has read P^T) with d = 128, columns of
+  // its own with d = 64; and of the dK accumulator.
+  static constexpr bool SEP_DQ = D == 64;
+  static constexpr uint32_t COL_DQ = SEP_DQ ? 320u : 0u;
+  static constexpr uint32_t COL_DK = 384u;
 };
 
 struct Bars {
@@ -137,12 +150,12 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   volatile int* abort_flag = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bhs = p.B * p.H;
   Unit u;
-  u.bh = blockIdx.x % bhs;
-  u.j = blockIdx.x / bhs;           // key block; small j first (most query blocks under causal)
   u.nb = (p.N + kBlk - 1) / kBlk;
   u.nq = u.nb;
+  const int bhs = p.B * p.H;
+  u.bh = blockIdx.x % bhs;
+  u.j = blockIdx.x / bhs;           // key block; small j first (most query blocks under causal)
   {
     int L = p.N;
     if (p.kv_len) {
@@ -264,6 +277,19 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       ok = ok && mbar_wait(&bars->do_full[0], 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
       if (ok) issue_dp(0);
+      auto issue_dk = [&](uint32_t aQ, int n) {
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ts(tb + C::COL_DK, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024),
+                 idKN, (n > 0 || kk > 0) ? 1u : 0u);
+      };
+      auto issue_dq = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          mma_ss(tb + C::COL_DQ, sw128_desc(aDS + 2048 * kk, kSub, 1024),
+                 sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
+        mma_commit(&bars->dq_full);
+      };
       int n = 0;
       for (int i = first; ok && i >= 0; ++n) {
         const int in = next_q(p, u, i);
@@ -276,41 +302,61 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         for (int kk = 0; kk < kBlk / 16; ++kk)
           mma_ts(tb + 256, tb + a_col(0, kk), sw128_desc(aDO + 2048 * kk, kSub, 1024), idKN,
                  (n > 0 || kk > 0) ? 1u : 0u);
-        // dQ_i = dS K_j first, into the S^T columns (P^T has been read by dV above): the dQ
-        // drain and the TMA reduce-adds behind it gate the next phase B, so they start as
-        // early as possible.
-        ok = mbar_wait(&bars->ds_ready, n & 1, abort_flag, p.err, p.wait_ns);
-        tc_fence_after();
-        if (!ok) break;
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tb, sw128_desc(aDS + 2048 * kk, kSub, 1024),
-                 sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
-        mma_commit(&bars->dq_full);
-        if (in >= 0) {
-          // S^T of the next block as soon as the drain has copied dQ_i out of its columns:
-          // the next phase A waits for nothing else.
-          ok = mbar_wait(&bars->dq_free, n & 1, abort_flag, p.err, p.wait_ns);
-          ok = ok && mbar_wait(&bars->q_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag,
-                               p.err, p.wait_ns);
+        if constexpr (C::SEP_DQ) {
+          if (in >= 0) {
+            // S^T of the next block over P^T(n), which dV(n) (issued before it) reads first;
+            // the softmax warps find it ready when they finish phase B(n).
+            ok = mbar_wait(&bars->q_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
+                           p.wait_ns);
+            tc_fence_after();
+            if (!ok) break;
+            issue_s(n + 1);
+          }
+          ok = mbar_wait(&bars->ds_ready, n & 1, abort_flag, p.err, p.wait_ns);
+          // dQ_i = dS K_j into its own columns (the drain has long copied out dQ(n-1)).
+          if (ok && n > 0) ok = mbar_wait(&bars->dq_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
           tc_fence_after();
           if (!ok) break;
-          issue_s(n + 1);
-        }
-        // dK += dS^T Q_i
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tb + 384, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024), idKN,
-                 (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->q_empty[n & 1]);
-        mma_commit(&bars->do_empty[n & 1]);
-        if (in >= 0) {
-          // dP^T of the next block over dP^T / dS^T of this one (read by phase B and dK).
-          ok = mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
-                         p.wait_ns);
+          issue_dq();
+          issue_dk(aQ, n);
+          mma_commit(&bars->q_empty[n & 1]);
+          mma_commit(&bars->do_empty[n & 1]);
+          if (in >= 0) {
+            ok = mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
+                           p.wait_ns);
+            tc_fence_after();
+            if (!ok) break;
+            issue_dp(n + 1);
+          }
+        } else {
+          // dQ_i = dS K_j first, into the S^T columns (P^T has been read by dV above): the dQ
+          // drain and the TMA reduce-adds behind it gate the next phase B, so they start as
+          // early as possible.
+          ok = mbar_wait(&bars->ds_ready, n & 1, abort_flag, p.err, p.wait_ns);
           tc_fence_after();
           if (!ok) break;
-          issue_dp(n + 1);
+          issue_dq();
+          if (in >= 0) {
+            // S^T of the next block as soon as the drain has copied dQ_i out of its columns:
+            // the next phase A waits for nothing else.
+            ok = mbar_wait(&bars->dq_free, n & 1, abort_flag, p.err, p.wait_ns);
+            ok = ok && mbar_wait(&bars->q_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag,
+                                 p.err, p.wait_ns);
+            tc_fence_after();
+            if (!ok) break;
+            issue_s(n + 1);
+          }
+          issue_dk(aQ, n);
+          mma_commit(&bars->q_empty[n & 1]);
+          mma_commit(&bars->do_empty[n & 1]);
+          if (in >= 0) {
+            // dP^T of the next block over dP^T / dS^T of this one (read by phase B and dK).
+            ok = mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
+                           p.wait_ns);
+            tc_fence_after();
+            if (!ok) break;
+            issue_dp(n + 1);
+          }
         }
         i = in;
       }
@@ -457,8 +503,10 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) dvals[e4] = D4[e4];
       ok = mbar_wait_warp(&bars->dp_full, n & 1, abort_flag, p.err, p.wait_ns);
-      // Two drain warps staged the previous dQ partial in the dS^T tile.
-      if (ok && n > 0) ok = mbar_wait_warp(&bars->sds_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
+      // d = 128: two drain warps staged the previous dQ partial in the dS^T tile; with d = 64
+      // the wait is taken just before the first store into the tile (below).
+      if (D == 128 && ok && n > 0)
+        ok = mbar_wait_warp(&bars->sds_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
       const uint64_t ks2 = f2_pack(p.drop_scale, p.drop_scale);
@@ -502,13 +550,20 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         // dS^T over this warpgroup's already-read dP^T columns, and into the swizzled
         // shared tile (row r, query columns 64w + 32h ...).
         tmem_st16(lane_base + 128 + 64 * w + 16 * h, dsp);
+        // d = 64: two drain warps staged the previous dQ partial in the dS^T tile: wait for
+        // their bulk reduce-adds to have read it before the first store into the tile.
+        if (D == 64 && h == 0 && n > 0)
+          ok = mbar_wait_warp(&bars->sds_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
+        if (ok) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint4 v4 = make_uint4(dsp[4 * g], dsp[4 * g + 1], dsp[4 * g + 2], dsp[4 * g + 3]);
-          *reinterpret_cast<uint4*>(sDS + sw128_offset(r, 64 * w + 32 * h + 8 * g)) = v4;
+          for (int g = 0; g < 4; ++g) {
+            uint4 v4 = make_uint4(dsp[4 * g], dsp[4 * g + 1], dsp[4 * g + 2], dsp[4 * g + 3]);
+            *reinterpret_cast<uint4*>(sDS + sw128_offset(r, 64 * w + 32 * h + 8 * g)) = v4;
+          }
         }
       }
       tmem_wait_st();
+      if (!ok) break;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->ds_ready);
@@ -523,7 +578,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       const bool store = key < p.N;
       const float mul = w == 0 ? p.scale : (DROP ? p.drop_scale : 1.f);
       __nv_bfloat16* dst = (w == 0 ? dk : dv) + (row_off + key) * D;
-      const uint32_t col0 = w == 0 ? 384u : 256u;
+      const uint32_t col0 = w == 0 ? C::COL_DK : 256u;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t a[32];
@@ -548,62 +603,63 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   } else if (warp >= 14) {
     if constexpr (D == 128) regs_release_to<kRegsControl>();  // idle control warps
   } else if (warp < 4) {
-    // ------------------------------------------------------------ dQ partials (query rows)
+    // ------------------------------------------------------------ dQ partials
     if constexpr (D == 128) regs_grow_to<kRegsDrain>();
     const uint32_t lane_base = tb + (static_cast<uint32_t>((warp & 3) << 5) << 16);
     bool ok = true;
     int n = 0;
+    const int wq = warp & 3;
     for (int i = first; ok && i >= 0; i = next_q(p, u, i)) {
       ok = mbar_wait_warp(&bars->dq_full, n & 1, abort_flag, p.err, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
-      // Lane = query row.  Each warp copies its 32 rows x d columns of the partial out of
-      // TMEM into [32 q][32 d] fp32 boxes with the 128-byte swizzle (16-byte stores, no bank
-      // conflicts), releases the TMEM columns at once, and hands the boxes to the TMA unit
-      // as bulk reduce-adds into the accumulator.  Warps 0-1 stage in this block's dO stage
-      // (its MMAs are done with it; the next dO load into it waits for these reads), warps
-      // 2-3 in the dS^T tile (the next phase B waits for these reads).
-      const int wq = warp & 3;
-      const int q0 = i * kBlk + 32 * wq;
-      uint8_t* st = wq < 2 ? sQ + (n & 1) * 2 * C::TILE + C::TILE + wq * (D / 32) * 4096
-                           : sDS + (wq - 2) * (D / 32) * 4096;
-      // The whole row slice comes out of TMEM in one load and the columns are released
-      // before any shared-memory store.
       {
-        uint32_t v[D];
-        if constexpr (D == 128) {
-          tmem_ld128_wait(lane_base, v);
-        } else {
-          tmem_ld64_wait(lane_base, lane_base + 32, v);
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->dq_free);
+        // Lane = query row.  Each warp copies its 32 rows x d columns of the partial out of
+        // TMEM into [32 q][32 d] fp32 boxes with the 128-byte swizzle (16-byte stores, no
+        // bank conflicts), releases the TMEM columns at once, and hands the boxes to the TMA
+        // unit as bulk reduce-adds into the accumulator.  Warps 0-1 stage in this block's dO
+        // stage (its MMAs are done with it; the next dO load into it waits for these reads),
+        // warps 2-3 in the dS^T tile (the next phase B waits for these reads).
+        const int q0 = i * kBlk + 32 * wq;
+        uint8_t* st = wq < 2 ? sQ + (n & 1) * 2 * C::TILE + C::TILE + wq * (D / 32) * 4096
+                             : sDS + (wq - 2) * (D / 32) * 4096;
+        {
+          uint32_t v[D];
+          if constexpr (D == 128) {
+            tmem_ld128_wait(lane_base + C::COL_DQ, v);
+          } else {
+            tmem_ld64_wait(lane_base + C::COL_DQ, lane_base + C::COL_DQ + 32, v);
+          }
+          tc_fence_before();
+          mbar_arrive(&bars->dq_free);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint8_t* row = st + cc * 4096 + lane * 128;
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint8_t* row = st + cc * 4096 + lane * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
-                make_uint4(v[32 * cc + 4 * j], v[32 * cc + 4 * j + 1], v[32 * cc + 4 * j + 2],
-                           v[32 * cc + 4 * j + 3]);
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
+                  make_uint4(v[32 * cc + 4 * j], v[32 * cc + 4 * j + 1],
+                             v[32 * cc + 4 * j + 2], v[32 * cc + 4 * j + 3]);
+          }
         }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        // The boxes in the dS^T tile go to the TMA first: the next phase B waits for them,
-        // while the dO stage is only needed again two blocks later.
-        bool go = true;
-        if (wq < 2) go = mbar_wait(&bars->sds_free, n & 1, abort_flag, p.err, p.wait_ns);
-        if (go && q0 < p.N) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // The boxes in the dS^T tile go to the TMA first: the next phase B waits for them,
+          // while the dO stage is only needed again two blocks later.
+          bool go = true;
+          if (wq < 2) go = mbar_wait(&bars->sds_free, n & 1, abort_flag, p.err, p.wait_ns);
+          if (go && q0 < p.N) {
 #pragma unroll 1
-          for (int cc = 0; cc < D / 32; ++cc) tma_reduce_add_3d(&mdq, st + cc * 4096, 32 * cc, q0, u.bh);
-          bulk_commit_group();
-          bulk_wait_group_read<0>();
+            for (int cc = 0; cc < D / 32; ++cc)
+              tma_reduce_add_3d(&mdq, st + cc * 4096, 32 * cc, q0, u.bh);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();
+          }
+          mbar_arrive(wq < 2 ? &bars->do_empty[n & 1] : &bars->sds_free);
         }
-        mbar_arrive(wq < 2 ? &bars->do_empty[n & 1] : &bars->sds_free);
+        __syncwarp();
       }
-      __syncwarp();
       ++n;
     }
   }
@@ -634,14 +690,14 @@ cudaError_t bwd_launch(const Problem& p, const void* q, const void* k, const voi
       !make_head_map(&mv, v, BH, p.N, D) || !make_head_map(&mdo, dO, BH, p.N, D) ||
       !make_acc_map(&mdq, dq_acc, BH, p.N, D))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64];  // per device; a race repeats the same call
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(bwd_sm103_kernel<D, DROP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true);
   }
   const int nkb = (p.N + kBlk - 1) / kBlk;
   dim3 grid(static_cast<unsigned>(BH) * nkb);

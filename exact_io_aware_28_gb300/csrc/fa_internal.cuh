@@ -27,8 +27,6 @@ struct Problem {
   int drop_threshold = 0;
   uint32_t drop_seed_lo = 0, drop_seed_hi = 0, drop_offset = 0;
   float drop_scale = 1.f;    // 256 / (256 - drop_threshold)
-  // Backward launch order: heads per group of CTAs (set by the backward launcher).
-  int head_group = 1;
 };
 
 // Bound of device-side waits: FA_WAIT_LIMIT_MS from the environment (read once), else 2 s.

@@ -178,12 +178,6 @@ __device__ __forceinline__ void bulk_wait_group_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Fire-and-forget fp32 add into global memory (relaxed, no return value).  A warp whose
-// lanes address 32 consecutive floats makes one fully coalesced 128-byte reduction.
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-
 // ------------------------------------------------------------------ tcgen05: TMEM
 
 // Allocate `ncols` (power of two >= 32) tensor-memory columns; the base address is
