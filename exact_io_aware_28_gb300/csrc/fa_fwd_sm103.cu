@@ -189,14 +189,24 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       int npv = 0;
       bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
-#define FA_ISSUE_S(slot)                                                                     \
-  do {                                                                                       \
-    _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                  \
-      const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kSub + (kk & 3) * 32) >> 4);   \
-      mma_ss(tS, dQ + off, dK + (slot) * kTileD + off, idS, kk > 0);                         \
-    }                                                                                        \
-    mma_commit(&bars->s_full[t]);                                                            \
-  } while (0)
+      // S_t = Q_t K^T of ring slot `slot`: groups of four MMAs, each group's descriptors
+      // built before its first MMA issues, so the four go out back to back.
+      auto issue_s = [&](int slot) {
+        const uint64_t dKs = dK + static_cast<uint64_t>(slot) * kTileD;
+#pragma unroll
+        for (int g = 0; g < D / 64; ++g) {
+          uint64_t da[4], db[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int kk = 4 * g + k;
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kSub + (kk & 3) * 32) >> 4);
+            da[k] = dQ + off;
+            db[k] = dKs + off;
+          }
+          mma_ss_x4(tS, da, db, idS, g > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full[t]);
+      };
       int j = next_any(p, u, -1, jend);
       if (ok && j >= 0) {
         const int ks = cs;
@@ -204,7 +214,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         if (++cs == C::NSTAGE) { cs = 0; ++cr; }
         tc_fence_after();
         if (ok) {
-          if (need(p, u, t, j)) FA_ISSUE_S(ks);
+          if (need(p, u, t, j)) issue_s(ks);
           mma_commit(&bars->kv_empty[ks]);
         }
       }
@@ -226,21 +236,28 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           ok = mbar_wait(&bars->p_full[t], npv & 1, abort_flag, p.err, p.wait_ns);
           tc_fence_after();
           if (!ok) break;
+          const uint64_t dVs = dV + static_cast<uint64_t>(vs) * kTileD;
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tO, tS + 8 * kk, dV + vs * kTileD + static_cast<uint64_t>((2048 * kk) >> 4),
-                   idO, (npv > 0 || kk > 0) ? 1u : 0u);
+          for (int g = 0; g < 2; ++g) {
+            uint32_t ta[4];
+            uint64_t db[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              ta[k] = tS + 8 * (4 * g + k);
+              db[k] = dVs + static_cast<uint64_t>((2048 * (4 * g + k)) >> 4);
+            }
+            mma_ts_x4(tO, ta, db, idO, (npv > 0 || g > 0) ? 1u : 0u);
+          }
           ++npv;
           if (j == last) mma_commit(&bars->o_done[t]);
         }
         mma_commit(&bars->kv_empty[vs]);
         if (jn >= 0) {
-          if (need(p, u, t, jn)) FA_ISSUE_S(ks);
+          if (need(p, u, t, jn)) issue_s(ks);
           mma_commit(&bars->kv_empty[ks]);
         }
         j = jn;
       }
-#undef FA_ISSUE_S
       // Drain: every MMA issued by either thread has completed before tensor memory is
       // released (the barrier counts one arrival per issuer).
       mma_commit(&bars->drain);

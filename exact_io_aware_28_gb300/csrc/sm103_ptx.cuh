@@ -397,6 +397,42 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// A group of 4 MMAs issued back to back from one asm statement, with every descriptor
+// (and TMEM address) computed before the first issue.  tcgen05.mma returns only when the
+// tensor pipe takes the instruction, so an address computation between two MMAs of a group
+// would leave the pipe idle meanwhile.  The first MMA accumulates iff acc0 != 0, the others
+// always accumulate.
+__device__ __forceinline__ void mma_ss_x4(uint32_t d_tmem, const uint64_t (&a)[4],
+                                          const uint64_t (&b)[4], uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\t"
+      "setp.ne.b32 t, %11, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, t;\n\t}" ::"r"(d_tmem), "r"(idesc),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(acc0), "r"(1u)
+      : "memory");
+}
+
+// Four MMAs with A read from TMEM (addresses a[k]), B from shared memory.
+__device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, const uint32_t (&a)[4],
+                                          const uint64_t (&b)[4], uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\t"
+      "setp.ne.b32 t, %11, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %9, %1, t;\n\t}" ::"r"(d_tmem), "r"(idesc),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(acc0), "r"(1u)
+      : "memory");
+}
+
 // Instruction descriptor, kind::f8f6f4: e4m3 A and B (format code 0), fp32 accumulator,
 // both operands K-major; same field positions as idesc_bf16.  One MMA contracts K = 32.
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
