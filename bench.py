@@ -435,9 +435,79 @@ def device_inputs(w, dev, x_cpu=None):
 
 
 # The other configurations timed in the default run's ``per_config`` block (the headline
-# workload itself is the line's value).
+# workload itself is the line's value), and the sequence-sharded schedule on one GPU.
 PER_CONFIG = ["tiny_fp32", "gpt2_causal", "bert_padded", "block_sparse", "long_causal_dropout",
-              "long_causal_fp8", "decode_llama8b"]
+              "long_causal_fp8", "decode_llama8b", "long_causal_chunks4"]
+CHUNKED = {"long_causal_chunks4": ("long_causal", 4)}
+
+
+def measure_chunked(fa, base: str, chunks: int, steps, warmup, world, dev):
+    """The sequence-sharded schedule with every rank in one process on one GPU: workload
+    ``base`` split into ``chunks`` equal contiguous chunks, the ring's forward (partial
+    forwards + merge) and backward per step, timed with CUDA events; and the merge kernel
+    alone on partials of the same size (HBM-bound)."""
+    from exact_io_aware_28_gb300 import seqshard
+    w = TRAIN_WORKLOADS[base]
+    x = device_inputs(w, dev)
+    n = w.N // chunks
+    cut = lambda t: [t[:, :, r * n:(r + 1) * n].contiguous() for r in range(chunks)]
+    qs, ks, vs, dos = cut(x.q), cut(x.k), cut(x.v), cut(x.do)
+    del x
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fwd = seqshard.chunked_forward(qs, ks, vs, w.causal, w.scale)
+        seqshard.chunked_backward(qs, ks, vs, [f[0] for f in fwd], [f[1] for f in fwd], dos,
+                                  w.causal, w.scale)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_error() != fa.FA_OK:
+        raise RuntimeError("device error word set during warm-up (chunked)")
+    sampler = ClockSampler(device_uuid(dev))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    for e0, e1 in evs:
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
+    fl = acc.flops(w.B, w.H, w.N, w.d, w.causal)["fwd_bwd"]
+    # the merge of `chunks` partials of one chunk's rows (what each rank merges)
+    parts = torch.randn((chunks, w.B, w.H, n, w.d), device=dev).to(torch.bfloat16)
+    lses = torch.randn((chunks, w.B, w.H, n), device=dev)
+    o = torch.empty((w.B, w.H, n, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, n), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        fa.fa_attn_merge(parts, lses, o, lse)
+    mevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)]
+    for e0, e1 in mevs:
+        e0.record(stream)
+        fa.fa_attn_merge(parts, lses, o, lse)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    mms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in mevs]))
+    rows = w.B * w.H * n
+    merge_bytes = chunks * rows * (w.d * 2 + 4) + rows * (w.d * 2 + 4)
+    pk = peaks()
+    return {"describe": f"{w.describe()} in {chunks} chunks of {n} rows, ring schedule in one "
+                        f"process", "value": fl / (ms.mean() * 1e-3) / 1e12,
+            "ms_per_step": float(ms.mean()), "timing": {"step_ms": summarize(ms)},
+            "clocks": clocks, "merge_gbs": merge_bytes / (mms * 1e-3) / 1e9,
+            "merge_frac_of_hbm": merge_bytes / (mms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "merge_ms": mms, "merge_bytes": merge_bytes,
+            # per rank r: v visible chunks (r + 1 under the causal mask, else all), v partial
+            # forwards + 1 merge; backward: preprocess, v mains with 2 accumulates each,
+            # 2 finishes, dQ convert
+            "launches": steps * sum(4 * v + 5 for v in
+                                    ((r + 1) if w.causal else chunks for r in range(chunks)))}
 
 
 def per_config(fa, args, world, dev, headline):
@@ -464,6 +534,15 @@ def per_config(fa, args, world, dev, headline):
             if w.dtype == "fp32":
                 entry["note"] = "fp32 CUDA-core path: no tensor-core peak applies"
                 entry.pop("pct_of_peak_burst")
+        elif name in CHUNKED:
+            base, nch = CHUNKED[name]
+            r = measure_chunked(fa, base, nch, steps, warmup, world, dev)
+            entry = {"workload": r["describe"], "metric": "fwd+bwd TFLOP/s", "value": r["value"],
+                     "pct_of_peak_burst": r["value"] / world / pk["bf16_tflops"],
+                     "ms_per_step": r["ms_per_step"], "merge_gbs": r["merge_gbs"],
+                     "merge_frac_of_hbm": r["merge_frac_of_hbm"], "merge_ms": r["merge_ms"],
+                     "timing": r["timing"], "clocks": r["clocks"], "launches": r["launches"],
+                     "steps": steps, "l2": "inputs larger than L2"}
         elif name in W.FP8_WORKLOADS:
             r = measure_fp8(fa, W.FP8_WORKLOADS[name], steps, warmup, world, dev)
             entry = {"workload": r["describe"], "metric": "fwd TFLOP/s (encode + e4m3 forward)",

@@ -107,7 +107,13 @@ def load() -> ctypes.CDLL:
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of ``t`` for the library (every tensor argument is device memory)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("the library takes CUDA tensors (device memory); got a "
+                         f"{t.device.type} tensor")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _dtype_code(t: torch.Tensor) -> int:

@@ -105,5 +105,7 @@ def test_per_config_covers_every_other_workload():
     # the four other scope configurations, the dropout and FP8 steps and decode
     assert set(W.ORDER) - {"long_causal"} <= names
     assert {"long_causal_dropout", "long_causal_fp8", "decode_llama8b"} <= names
+    assert "long_causal_chunks4" in names        # the sequence-sharded schedule (one GPU)
     for n in names:
-        assert n in bench.TRAIN_WORKLOADS or n in W.FP8_WORKLOADS or n in W.DECODE_WORKLOADS
+        assert (n in bench.TRAIN_WORKLOADS or n in W.FP8_WORKLOADS or n in W.DECODE_WORKLOADS
+                or n in bench.CHUNKED)

@@ -266,3 +266,72 @@ def test_dropout_python_binding_checks_the_threshold():
 ])
 def test_dropout_random_bytes_rejects_bad_sizes(args, code):
     assert fa.load().fa_dropout_random_bytes(*args, 1, 0, None) == code
+
+
+# ------------------------------------------------------------------ sequence sharding
+
+def merge(**kw):
+    args = dict(parts=A, lses=A, S=4, o=A, lse=A, B=1, H=2, N=128, d=128, dtype=fa.FA_BF16)
+    args.update(kw)
+    return fa.load().fa_attn_merge(args["parts"], args["lses"], args["S"], args["o"],
+                                   args["lse"], args["B"], args["H"], args["N"], args["d"],
+                                   args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"S": 0}, fa.FA_ERR_INVALID_ARG),
+    ({"S": fa.FA_MERGE_MAX_PARTS + 1}, fa.FA_ERR_INVALID_ARG),
+    ({"B": 0}, fa.FA_ERR_INVALID_ARG),
+    ({"N": -1}, fa.FA_ERR_INVALID_ARG),
+    ({"d": 96}, fa.FA_ERR_UNSUPPORTED),
+    ({"dtype": 5}, fa.FA_ERR_INVALID_ARG),
+    ({"parts": None}, fa.FA_ERR_INVALID_ARG),
+    ({"lse": None}, fa.FA_ERR_INVALID_ARG),
+    ({"o": A + 8}, fa.FA_ERR_INVALID_ARG),
+    ({"lses": A + 2}, fa.FA_ERR_INVALID_ARG),
+])
+def test_merge_rejects_bad_arguments(kw, code):
+    assert merge(**kw) == code
+
+
+@pytest.mark.parametrize("fn", ["fa_grad_accumulate", "fa_grad_finish"])
+@pytest.mark.parametrize("args,code", [
+    ((None, A, 64, fa.FA_BF16), fa.FA_ERR_INVALID_ARG),
+    ((A, None, 64, fa.FA_BF16), fa.FA_ERR_INVALID_ARG),
+    ((A, A, 0, fa.FA_BF16), fa.FA_ERR_INVALID_ARG),
+    ((A, A, 66, fa.FA_BF16), fa.FA_ERR_INVALID_ARG),     # not a multiple of 4
+    ((A, A, 64, 9), fa.FA_ERR_INVALID_ARG),
+])
+def test_gradient_sums_reject_bad_arguments(fn, args, code):
+    assert getattr(fa.load(), fn)(*args, None) == code
+
+
+def test_gradient_sums_check_alignment():
+    lib = fa.load()
+    # fp32 sums are 16-byte aligned; bf16 contributions need 8 bytes, fp32 ones 16
+    assert lib.fa_grad_accumulate(A + 8, A, 64, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_grad_accumulate(A, A + 8, 64, fa.FA_FP32, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_grad_finish(A + 4, A, 64, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_grad_finish(A, A + 8, 64, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_merge_binding_checks_shapes():
+    import torch
+    parts = torch.empty((2, 1, 1, 4, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_attn_merge(parts, torch.empty((2, 1, 1, 5)), torch.empty((1, 1, 4, 64),
+                                                                       dtype=torch.bfloat16),
+                         torch.empty((1, 1, 4)))
+    with pytest.raises(TypeError):
+        fa.fa_attn_merge(parts, torch.empty((2, 1, 1, 4)), torch.empty((1, 1, 4, 64)),
+                         torch.empty((1, 1, 4)))
+
+
+def test_binding_refuses_host_tensors():
+    # A host pointer reaching a kernel would fault the GPU: the binding refuses it first.
+    import torch
+    q = torch.zeros((1, 1, 8, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        fa.fa_fwd(q, q, q, q.clone(), torch.zeros((1, 1, 8)))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        fa.fa_grad_accumulate(torch.zeros(8), torch.zeros(8, dtype=torch.bfloat16))
