@@ -64,15 +64,41 @@ merge_kernel(const T* __restrict__ o_parts, const float* __restrict__ lse_parts,
   for (long long r0 = warp * RPW; r0 < rows; r0 += nwarps * RPW) {
     const long long row = r0 + sub;
     if (row >= rows) continue;
-    // m = max_k lse_k, then the weights e^{lse_k - m} and their sum.
+    // m = max_k lse_k, then the weights e^{lse_k - m} and their sum; four parts' loads are
+    // in flight at a time.
     float m = -INFINITY;
-    for (int k = 0; k < S; ++k) m = fmaxf(m, __ldg(lse_parts + k * rows + row));
+    int k = 0;
+    for (; k + 4 <= S; k += 4) {
+      float l[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) l[t] = __ldg(lse_parts + (k + t) * rows + row);
+      m = fmaxf(m, fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3])));
+    }
+    for (; k < S; ++k) m = fmaxf(m, __ldg(lse_parts + k * rows + row));
     float acc[VEC];
 #pragma unroll
     for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
     float total = 0.f;
     if (m != -INFINITY) {
-      for (int k = 0; k < S; ++k) {
+      k = 0;
+      for (; k + 4 <= S; k += 4) {
+        float l[4], x[4][VEC];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          l[t] = __ldg(lse_parts + (k + t) * rows + row);
+          V16<T>::load(o_parts + ((k + t) * rows + row) * D + part * VEC, x[t]);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          // a part without visible keys (lse = -inf) contributes nothing, whatever its O row
+          if (l[t] == -INFINITY) continue;
+          const float wk = expf(l[t] - m);
+          total += wk;
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) acc[i] = fmaf(wk, x[t][i], acc[i]);
+        }
+      }
+      for (; k < S; ++k) {
         const float lk = __ldg(lse_parts + k * rows + row);
         if (lk == -INFINITY) continue;
         const float wk = expf(lk - m);
