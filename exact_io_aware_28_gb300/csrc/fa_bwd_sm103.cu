@@ -156,14 +156,6 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   const int bhs = p.B * p.H;
   u.bh = blockIdx.x % bhs;
   u.j = blockIdx.x / bhs;           // key block; small j first (most query blocks under causal)
-  {
-    int L = p.N;
-    if (p.kv_len) {
-      L = p.kv_len[u.bh / p.H];
-      L = L < 0 ? 0 : (L > p.N ? p.N : L);
-    }
-    u.L = L;
-  }
 
   if (tid == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -197,6 +189,18 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = bars->tmem_base;
+  // Set-up done; global memory (the key lengths and the block mask included) only after the
+  // previous kernel in the stream has completed.
+  griddep_wait();
+  griddep_launch_dependents();
+  {
+    int L = p.N;
+    if (p.kv_len) {
+      L = p.kv_len[u.bh / p.H];
+      L = L < 0 ? 0 : (L > p.N ? p.N : L);
+    }
+    u.L = L;
+  }
   const int first = next_q(p, u, -1);
   // Registers (d = 128): launched with 128 per thread (512 threads).  The producer / MMA
   // warpgroup (warps 12-15) gives 72 of them back; the dQ drain warpgroup (warps 0-3) takes
@@ -701,10 +705,9 @@ cudaError_t bwd_launch(const Problem& p, const void* q, const void* k, const voi
   }
   const int nkb = (p.N + kBlk - 1) / kBlk;
   dim3 grid(static_cast<unsigned>(BH) * nkb);
-  bwd_sm103_kernel<D, DROP><<<grid, kThreads, Cfg<D>::SMEM, s>>>(
-      mq, mk, mv, mdo, mdq, lse, Dsum, dq_acc, static_cast<__nv_bfloat16*>(dk),
-      static_cast<__nv_bfloat16*>(dv), p);
-  return cudaGetLastError();
+  return launch_dependent(bwd_sm103_kernel<D, DROP>, grid, dim3(kThreads), Cfg<D>::SMEM, s, mq,
+                          mk, mv, mdo, mdq, lse, Dsum, dq_acc, static_cast<__nv_bfloat16*>(dk),
+                          static_cast<__nv_bfloat16*>(dv), p);
 }
 
 }  // namespace

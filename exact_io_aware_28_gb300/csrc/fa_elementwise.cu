@@ -11,6 +11,7 @@
 // Both read and write every byte exactly once with 16-byte vector accesses and a
 // grid-stride loop over a grid sized to the SM count.
 #include "fa_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace fa {
 namespace {
@@ -45,6 +46,9 @@ preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dO, float* __re
   constexpr int VEC = Vec<T>::n;
   constexpr int TPR = D / VEC;           // 8 or 16 (bf16), 16 or 32 (fp32)
   constexpr int RPW = 32 / TPR;          // rows per warp per iteration
+  // O of the forward just launched, and the dQ accumulator the previous convert read.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -75,6 +79,8 @@ preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dO, float* __re
 __global__ void __launch_bounds__(256)
 dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, float scale,
                   long long n8) {
+  ptx::griddep_wait();   // the backward main kernel's reduce-adds
+  ptx::griddep_launch_dependents();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += stride) {
     const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
@@ -98,9 +104,8 @@ cudaError_t preprocess_typed(const Problem& p, const void* o, const void* dO, fl
   long long blocks = (warps_needed + 7) / 8;
   const long long cap = (long long)sm_count() * 8;  // 8 CTAs of 256 threads per SM
   if (blocks > cap) blocks = cap;
-  preprocess_kernel<T, D><<<(unsigned)blocks, 256, 0, s>>>((const T*)o, (const T*)dO, Dsum,
-                                                          dq_acc, rows);
-  return cudaGetLastError();
+  return launch_dependent(preprocess_kernel<T, D>, dim3((unsigned)blocks), dim3(256), 0, s,
+                          (const T*)o, (const T*)dO, Dsum, dq_acc, rows);
 }
 
 }  // namespace
@@ -119,8 +124,8 @@ cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, void* dq, c
   long long blocks = (n8 + 255) / 256;
   const long long cap = (long long)sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  dq_convert_kernel<<<(unsigned)blocks, 256, 0, s>>>(dq_acc, (__nv_bfloat16*)dq, p.scale, n8);
-  return cudaGetLastError();
+  return launch_dependent(dq_convert_kernel, dim3((unsigned)blocks), dim3(256), 0, s, dq_acc,
+                          (__nv_bfloat16*)dq, p.scale, n8);
 }
 
 }  // namespace fa

@@ -94,17 +94,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   Unit u;
   u.bh = blockIdx.x % bhs;
   u.q0 = (nqb - 1 - static_cast<int>(blockIdx.x / bhs)) * 2 * kBlk;
-  {
-    int L = p.N;
-    if (p.kv_len) {
-      const int b = u.bh / p.H;
-      L = p.kv_len[b];
-      L = L < 0 ? 0 : (L > p.N ? p.N : L);
-    }
-    u.L = L;
-  }
   u.nb = (p.N + kBlk - 1) / kBlk;
-  const int jend = key_blocks(p, u);
 
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
@@ -131,6 +121,20 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = bars->tmem_base;
+  // Set-up done; global memory (the key lengths included) only after the previous kernel in
+  // the stream has completed.
+  griddep_wait();
+  griddep_launch_dependents();
+  {
+    int L = p.N;
+    if (p.kv_len) {
+      const int b = u.bh / p.H;
+      L = p.kv_len[b];
+      L = L < 0 ? 0 : (L > p.N ? p.N : L);
+    }
+    u.L = L;
+  }
+  const int jend = key_blocks(p, u);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -553,8 +557,8 @@ static cudaError_t fwd_launch(const Problem& p, const void* q, const void* k, co
   }
   const int nqb = (p.N + 255) / 256;
   dim3 grid(static_cast<unsigned>(BH) * nqb);
-  fwd_sm103_kernel<D, DROP><<<grid, kThreads, Cfg<D>::SMEM, s>>>(mq, mk, mv, mo, lse, p);
-  return cudaGetLastError();
+  return launch_dependent(fwd_sm103_kernel<D, DROP>, grid, dim3(kThreads), Cfg<D>::SMEM, s, mq,
+                          mk, mv, mo, lse, p);
 }
 
 cudaError_t launch_fwd_sm103(const Problem& p, const void* q, const void* k, const void* v,

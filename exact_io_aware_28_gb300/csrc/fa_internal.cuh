@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "fa.h"
 
 namespace fa {
@@ -34,6 +36,27 @@ unsigned long long wait_limit_ns();
 
 // Device error codes written into the error word (match fa_status).
 constexpr int kErrTimeout = FA_ERR_TIMEOUT;
+
+// Launch of a kernel of the training step (forward, preprocess, backward main, dQ convert)
+// with programmatic stream serialization: it may be scheduled while the previous kernel in
+// the stream drains, runs its set-up (barriers, tensor memory, descriptor prefetch), and waits
+// in griddep_wait before it touches global memory.  Every such kernel calls griddep_wait in
+// every CTA before it can exit, so completion stays ordered along the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers.  Each returns cudaSuccess or the launch error.
 cudaError_t launch_fwd_simt(const Problem& p, fa_dtype dt, const void* q, const void* k,

@@ -110,6 +110,21 @@ __device__ __forceinline__ void regs_grow_to() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// ------------------------------------------------------------------ dependent launch
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization
+// may start while the previous kernel in the stream is still running; griddep_wait blocks
+// until every grid it depends on has completed and its memory operations are visible (a
+// no-op for a kernel launched without the attribute).  griddep_launch_dependents lets the
+// next such kernel in the stream start its own launch once every CTA of this grid has made
+// the call or exited.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
