@@ -65,3 +65,27 @@ def test_dropout_and_plain_steps_interleaved():
     assert fa.fa_device_error() == fa.FA_OK
     for x, out in plain:
         compare(out, run_oracle(x), "bf16")
+
+
+def test_foreign_kernels_before_and_after():
+    # Inputs written by torch kernels launched just before the forward, outputs read by torch
+    # kernels just after the backward, all on the current stream without synchronisation: the
+    # library's kernels must wait for the writers and finish before the readers.
+    B, H, N, d = 1, 2, 320, 128
+    w = W.custom("chain", B, H, N, d, "bf16", causal=True)
+    x = W.make_inputs(w, seed=51, device="cuda")
+    ref = run_oracle(x)
+    torch.cuda.synchronize()
+    q2, k2, v2, do2 = (torch.zeros_like(t) for t in (x.q, x.k, x.v, x.do))
+    for dst, src in zip((q2, k2, v2, do2), (x.q, x.k, x.v, x.do)):
+        dst.add_(src)                      # a torch kernel writes each input
+    o = torch.empty_like(q2)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = (torch.empty_like(q2) for _ in range(3))
+    ws = fa.alloc_workspace(B, H, N, d, "cuda")
+    fa.fa_fwd(q2, k2, v2, o, lse, True)
+    fa.fa_bwd(q2, k2, v2, o, lse, do2, dq, dk, dv, ws, True)
+    copies = [t.clone() for t in (o, lse, dq, dk, dv)]   # torch kernels read each output
+    torch.cuda.synchronize()
+    assert fa.fa_device_error() == fa.FA_OK
+    compare(tuple(copies), ref, "bf16")
