@@ -27,6 +27,11 @@
  * by the caller; the library allocates no device memory per call.  Tensor pointers must be
  * 16-byte aligned.  Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  * NULL is the legacy default stream): outputs are valid once the stream has synchronised.
+ * The kernels of fa_fwd, fa_fwd_dropout and the three backward stages are launched with
+ * programmatic stream serialization: one may be scheduled while the previous kernel in the
+ * stream is still running, but it reads and writes global memory only after that kernel
+ * has completed, so stream order holds as for ordinary launches (also inside a captured
+ * CUDA graph, which keeps the attribute).
  *
  * Errors: arguments are validated on the host before any launch; a failed check returns
  * FA_ERR_INVALID_ARG (bad pointer, size, alignment, dtype, workspace) or FA_ERR_UNSUPPORTED
