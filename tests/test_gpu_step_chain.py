@@ -89,3 +89,37 @@ def test_foreign_kernels_before_and_after():
     torch.cuda.synchronize()
     assert fa.fa_device_error() == fa.FA_OK
     compare(tuple(copies), ref, "bf16")
+
+
+def test_training_step_captured_in_a_cuda_graph():
+    # The chained launches captured by stream capture and replayed: each replay on new inputs
+    # copied into the captured buffers matches the oracle.
+    B, H, N, d = 1, 2, 384, 128
+    w = W.custom("chain", B, H, N, d, "bf16", causal=True)
+    xs = [W.make_inputs(w, seed=61 + s, device="cuda") for s in range(3)]
+    q, k, v, do = (t.clone() for t in (xs[0].q, xs[0].k, xs[0].v, xs[0].do))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = fa.alloc_workspace(B, H, N, d, "cuda")
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, True)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, True)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()                                 # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for x in xs[1:]:
+        for dst, src in zip((q, k, v, do), (x.q, x.k, x.v, x.do)):
+            dst.copy_(src)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert fa.fa_device_error() == fa.FA_OK
+        compare((o, lse, dq, dk, dv), run_oracle(x), "bf16")
