@@ -16,26 +16,27 @@
 // the causal mask, mask[i][j] = 1 under a block mask), accumulating dK_j, dV_j in tensor
 // memory and adding each dQ_i partial to an fp32 accumulator in global memory.
 // Per query block the tensor pipe runs five MMAs (all M = 128, bf16 in, fp32 out):
-//   S^T  = K_j Q_i^T   (A: K_j K-major smem,    B: Q_i K-major smem)    -> TMEM R0
-//   dP^T = V_j dO_i^T  (A: V_j K-major smem,    B: dO_i K-major smem)   -> TMEM R1
+//   S^T  = K_j Q_i^T   (A: K_j K-major smem,    B: Q_i K-major smem)    -> TMEM Ra
+//   dP^T = V_j dO_i^T  (A: V_j K-major smem,    B: dO_i K-major smem)   -> TMEM Rb
 //   dV  += P^T dO_i    (A: P^T bf16 in TMEM,    B: dO_i MN-major smem)  -> TMEM [256,256+d)
 //   dK  += dS^T Q_i    (A: dS^T bf16 in TMEM,   B: Q_i MN-major smem)   -> TMEM dK columns
 //   dQ_i = dS K_j      (A: dS^T MN-major smem,  B: K_j MN-major smem)   -> TMEM dQ columns
 // with R0 = [0,128) and R1 = [128,256).  P^T is written over already-read S^T columns and
-// dS^T over already-read dP^T columns.  With d = 128 the dQ partial (TMEM lane = query row)
-// goes into R0 once dV has read P^T there (dK at [384,512)); with d = 64 it has columns of its
-// own, [320,384) (dK at [384,448)).
+// dS^T over already-read dP^T columns.  With d = 128 the two regions swap roles every block:
+// block n has Ra = R[n % 2], Rb the other, and its dQ partial (TMEM lane = query row) goes
+// into Ra once dV has read P^T there (dK at [384,512)).  With d = 64, Ra = R0, Rb = R1 and
+// the dQ partial has columns of its own, [320,384) (dK at [384,448)).
 // Warps (16): 0-3 the dQ drain, 4-7 and 8-11 two warpgroups that each take 64 of the 128
 // query columns of every key row (phase A: P^T from S^T; phase B: dS^T from dP^T), 12 TMA
 // producer (K_j, V_j once; Q_i and dO_i through two-stage rings) and tensor-memory
 // allocation, 13 MMA issuer, 14-15 idle.  The drain copies each dQ_i partial out of TMEM
 // into 128-byte-swizzled [32 rows][32 columns] fp32 boxes in shared memory and adds them to
 // the fp32 accumulator in global memory with TMA bulk reduce-adds.
-// MMA issue order per block n, d = 128: dV(n), dQ(n), S^T(n+1), dK(n), dP^T(n+1).  The dQ
+// MMA issue order per block n, d = 128: dV(n), dQ(n), dK(n), S^T(n+1), dP^T(n+1).  The dQ
 // drain and the bulk reduce-adds behind it decide when the next phase B may reuse the dS
-// tile, so dQ(n) goes first once phase B(n) is done; the drain copies the whole partial out
-// of TMEM in one load, and S^T(n+1) follows as soon as it has, so the next phase A starts
-// early; dP^T(n+1) needs only dK(n) to have read dS^T(n).
+// tile, so dQ(n) goes first once phase B(n) is done.  S^T(n+1) goes into Rb(n) as soon as
+// dK(n) (issued before it) has read dS^T(n) there, without waiting for the drain; dP^T(n+1)
+// goes into Ra(n) once the drain has copied the partial out of it in one load.
 // d = 64: dV(n), S^T(n+1), then (after phase B(n)) dQ(n), dK(n), dP^T(n+1): with dQ in columns
 // of its own nothing waits for the drain, and S^T(n+1) goes into R0 as soon as dV(n) (issued
 // before it; one thread's MMAs run in issue order) has read P^T(n), so it is ready when the
@@ -61,10 +62,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kProducerWarp = 12;  // also allocates tensor memory
 constexpr int kMmaWarp = 13;       // warps 14-15 idle
 constexpr int kThreads = 512;
-// Registers per thread after reallocation (d = 128; launched with 128).
+// Registers per thread after reallocation (d = 128; launched with 128): the MMA issuer takes
+// the TMEM region of each block as a runtime address and needs more than 56.
 constexpr int kRegsDrain = 168;    // warps 0-3
-constexpr int kRegsSoftmax = 144;  // warps 4-11
-constexpr int kRegsControl = 56;   // warps 12-15
+constexpr int kRegsSoftmax = 136;  // warps 4-11
+constexpr int kRegsControl = 72;   // warps 12-15
 
 template <int D>
 struct Cfg {
@@ -189,6 +191,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = bars->tmem_base;
+  // d = 128: the two 128-column regions swap roles every block -- S^T, P^T and then the dQ
+  // partial of block n in R[n % 2], dP^T and dS^T in the other -- so that S^T of the next
+  // block need not wait for the drain; d = 64 keeps S^T in R0 and dP^T in R1.
+  auto s_reg = [](int n) { return C::SEP_DQ ? 0u : static_cast<uint32_t>(n & 1) * 128u; };
+  auto d_reg = [&](int n) { return 128u - s_reg(n); };
   // Set-up done; global memory (the key lengths and the block mask included) only after the
   // previous kernel in the stream has completed.
   griddep_wait();
@@ -203,10 +210,10 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   }
   const int first = next_q(p, u, -1);
   // Registers (d = 128): launched with 128 per thread (512 threads).  The producer / MMA
-  // warpgroup (warps 12-15) gives 72 of them back; the dQ drain warpgroup (warps 0-3) takes
+  // warpgroup (warps 12-15) gives 56 of them back; the dQ drain warpgroup (warps 0-3) takes
   // 40, so a drain warp can hold a whole 128-column dQ row slice, and each softmax
-  // warpgroup 16, so phase A can load all 64 of its S^T columns at once:
-  // 4 x 32 x (168 + 144 + 144 + 56) = 512 x 128.  With d = 64 everything fits as launched.
+  // warpgroup 8, so phase A can load all 64 of its S^T columns at once:
+  // 4 x 32 x (168 + 136 + 136 + 72) = 512 x 128.  With d = 64 everything fits as launched.
   static_assert(kThreads == 512 && kRegsDrain + 2 * kRegsSoftmax + kRegsControl == 4 * 128, "register split");
 
   if (warp == kProducerWarp) {
@@ -255,21 +262,21 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       auto a_col = [](uint32_t region, int kk) {
         return region + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4));
       };
-      auto issue_s = [&](int n) {
+      auto issue_s = [&](int n, uint32_t tdst) {
         const uint32_t aQ = q_addr(n);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
-          mma_ss(tb, sw128_desc(aK + off, 16, 1024), sw128_desc(aQ + off, 16, 1024), idSS, kk > 0);
+          mma_ss(tdst, sw128_desc(aK + off, 16, 1024), sw128_desc(aQ + off, 16, 1024), idSS, kk > 0);
         }
         mma_commit(&bars->s_full);
       };
-      auto issue_dp = [&](int n) {
+      auto issue_dp = [&](int n, uint32_t tdst) {
         const uint32_t aDO = q_addr(n) + C::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
-          mma_ss(tb + 128, sw128_desc(aV + off, 16, 1024), sw128_desc(aDO + off, 16, 1024), idSS,
+          mma_ss(tdst, sw128_desc(aV + off, 16, 1024), sw128_desc(aDO + off, 16, 1024), idSS,
                  kk > 0);
         }
         mma_commit(&bars->dp_full);
@@ -277,20 +284,21 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.err, p.wait_ns);
       ok = ok && mbar_wait(&bars->q_full[0], 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
-      if (ok) issue_s(0);
+      if (ok) issue_s(0, tb);
       ok = ok && mbar_wait(&bars->do_full[0], 0, abort_flag, p.err, p.wait_ns);
       tc_fence_after();
-      if (ok) issue_dp(0);
-      auto issue_dk = [&](uint32_t aQ, int n) {
+      if (ok) issue_dp(0, tb + 128);
+      // tds: TMEM address of the region holding dS^T (bf16 pairs as the A operand).
+      auto issue_dk = [&](uint32_t aQ, int n, uint32_t tds) {
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tb + C::COL_DK, tb + a_col(128, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024),
+          mma_ts(tb + C::COL_DK, tds + a_col(0, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024),
                  idKN, (n > 0 || kk > 0) ? 1u : 0u);
       };
-      auto issue_dq = [&]() {
+      auto issue_dq = [&](uint32_t tdst) {
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tb + C::COL_DQ, sw128_desc(aDS + 2048 * kk, kSub, 1024),
+          mma_ss(tdst, sw128_desc(aDS + 2048 * kk, kSub, 1024),
                  sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
         mma_commit(&bars->dq_full);
       };
@@ -298,13 +306,15 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       for (int i = first; ok && i >= 0; ++n) {
         const int in = next_q(p, u, i);
         const uint32_t aQ = q_addr(n), aDO = aQ + C::TILE;
+        const uint32_t par = s_reg(n);   // this block's S^T region (0 or 128)
+        const uint32_t tP = tb + par;     // ... where P^T is
         // dV += P^T dO_i  (dO_i was waited for before dP^T(n))
         ok = mbar_wait(&bars->p_ready, n & 1, abort_flag, p.err, p.wait_ns);
         tc_fence_after();
         if (!ok) break;
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tb + 256, tb + a_col(0, kk), sw128_desc(aDO + 2048 * kk, kSub, 1024), idKN,
+          mma_ts(tb + 256, tP + a_col(0, kk), sw128_desc(aDO + 2048 * kk, kSub, 1024), idKN,
                  (n > 0 || kk > 0) ? 1u : 0u);
         if constexpr (C::SEP_DQ) {
           if (in >= 0) {
@@ -314,15 +324,15 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                            p.wait_ns);
             tc_fence_after();
             if (!ok) break;
-            issue_s(n + 1);
+            issue_s(n + 1, tb);
           }
           ok = mbar_wait(&bars->ds_ready, n & 1, abort_flag, p.err, p.wait_ns);
           // dQ_i = dS K_j into its own columns (the drain has long copied out dQ(n-1)).
           if (ok && n > 0) ok = mbar_wait(&bars->dq_free, (n - 1) & 1, abort_flag, p.err, p.wait_ns);
           tc_fence_after();
           if (!ok) break;
-          issue_dq();
-          issue_dk(aQ, n);
+          issue_dq(tb + C::COL_DQ);
+          issue_dk(aQ, n, tb + 128u);
           mma_commit(&bars->q_empty[n & 1]);
           mma_commit(&bars->do_empty[n & 1]);
           if (in >= 0) {
@@ -330,36 +340,33 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                            p.wait_ns);
             tc_fence_after();
             if (!ok) break;
-            issue_dp(n + 1);
+            issue_dp(n + 1, tb + 128);
           }
         } else {
-          // dQ_i = dS K_j first, into the S^T columns (P^T has been read by dV above): the dQ
-          // drain and the TMA reduce-adds behind it gate the next phase B, so they start as
-          // early as possible.
+          // dQ_i = dS K_j first, into this block's S^T region (dV has read P^T there): its drain
+          // and the TMA reduce-adds behind it gate the next phase B.  dK reads dS^T from the
+          // other region, and S^T of the next block goes over it at once (one thread's MMAs run
+          // in issue order); dP^T of the next block takes this block's region once the drain
+          // has copied dQ_i out of it.
           ok = mbar_wait(&bars->ds_ready, n & 1, abort_flag, p.err, p.wait_ns);
           tc_fence_after();
           if (!ok) break;
-          issue_dq();
-          if (in >= 0) {
-            // S^T of the next block as soon as the drain has copied dQ_i out of its columns:
-            // the next phase A waits for nothing else.
-            ok = mbar_wait(&bars->dq_free, n & 1, abort_flag, p.err, p.wait_ns);
-            ok = ok && mbar_wait(&bars->q_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag,
-                                 p.err, p.wait_ns);
-            tc_fence_after();
-            if (!ok) break;
-            issue_s(n + 1);
-          }
-          issue_dk(aQ, n);
+          issue_dq(tP);
+          issue_dk(aQ, n, tb + 128u - par);
           mma_commit(&bars->q_empty[n & 1]);
           mma_commit(&bars->do_empty[n & 1]);
           if (in >= 0) {
-            // dP^T of the next block over dP^T / dS^T of this one (read by phase B and dK).
-            ok = mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
+            ok = mbar_wait(&bars->q_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, p.err,
                            p.wait_ns);
             tc_fence_after();
             if (!ok) break;
-            issue_dp(n + 1);
+            issue_s(n + 1, tb + 128u - par);
+            ok = mbar_wait(&bars->dq_free, n & 1, abort_flag, p.err, p.wait_ns);
+            ok = ok && mbar_wait(&bars->do_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag,
+                                 p.err, p.wait_ns);
+            tc_fence_after();
+            if (!ok) break;
+            issue_dp(n + 1, tb + par);
           }
         }
         i = in;
@@ -458,7 +465,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       const bool masked = diag || !key_live;
       // Both halves of this warpgroup's S^T columns in one round trip.
       uint32_t sva[64];
-      tmem_ld64_wait(lane_base + 64 * w, lane_base + 64 * w + 32, sva);
+      const uint32_t sR = s_reg(n), dR = d_reg(n);
+      tmem_ld64_wait(lane_base + sR + 64 * w, lane_base + sR + 64 * w + 32, sva);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t* sv = sva + 32 * h;
@@ -493,9 +501,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           const uint32_t b = static_cast<uint32_t>(zbits >> (2 * e)) & 3u;
           pz[e] = pp[e] & ((b & 1u ? 0x0000FFFFu : 0u) | (b & 2u ? 0xFFFF0000u : 0u));
         }
-        tmem_st32(lane_base + 64 * w, pz);
+        tmem_st32(lane_base + sR + 64 * w, pz);
       } else {
-        tmem_st32(lane_base + 64 * w, pp);
+        tmem_st32(lane_base + sR + 64 * w, pp);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -521,7 +529,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) dvals[e4] = D4[8 + e4];
         }
-        tmem_ld32_wait(lane_base + 128 + 64 * w + 32 * h, dpv);
+        tmem_ld32_wait(lane_base + dR + 64 * w + 32 * h, dpv);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 nd = dvals[e4];   // -D
@@ -553,7 +561,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
         // dS^T over this warpgroup's already-read dP^T columns, and into the swizzled
         // shared tile (row r, query columns 64w + 32h ...).
-        tmem_st16(lane_base + 128 + 64 * w + 16 * h, dsp);
+        tmem_st16(lane_base + dR + 64 * w + 16 * h, dsp);
         // d = 64: two drain warps staged the previous dQ partial in the dS^T tile: wait for
         // their bulk reduce-adds to have read it before the first store into the tile.
         if (D == 64 && h == 0 && n > 0)
@@ -630,7 +638,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         {
           uint32_t v[D];
           if constexpr (D == 128) {
-            tmem_ld128_wait(lane_base + C::COL_DQ, v);
+            tmem_ld128_wait(lane_base + s_reg(n), v);
           } else {
             tmem_ld64_wait(lane_base + C::COL_DQ, lane_base + C::COL_DQ + 32, v);
           }
