@@ -262,23 +262,30 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       auto a_col = [](uint32_t region, int kk) {
         return region + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4));
       };
-      auto issue_s = [&](int n, uint32_t tdst) {
-        const uint32_t aQ = q_addr(n);
+      // Groups of four MMAs from one asm statement, descriptors built first (advanced from
+      // their k = 0 form by the byte offset >> 4), so that the four go out back to back.
+      auto issue_ss_k = [&](uint32_t tdst, uint32_t aA, uint32_t aB) {   // K-major A and B
+        const uint64_t dA = sw128_desc(aA, 16, 1024), dB = sw128_desc(aB, 16, 1024);
+        const uint32_t a_lo = static_cast<uint32_t>(dA), b_lo = static_cast<uint32_t>(dB);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
-          mma_ss(tdst, sw128_desc(aK + off, 16, 1024), sw128_desc(aQ + off, 16, 1024), idSS, kk > 0);
+        for (int g = 0; g < D / 64; ++g) {
+          uint32_t da[4], db[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t off = static_cast<uint32_t>((g * kSub + k * 32) >> 4);
+            da[k] = a_lo + off;
+            db[k] = b_lo + off;
+          }
+          mma_ss_x4_lo(tdst, da, static_cast<uint32_t>(dA >> 32), db,
+                       static_cast<uint32_t>(dB >> 32), idSS, g > 0 ? 1u : 0u);
         }
+      };
+      auto issue_s = [&](int n, uint32_t tdst) {
+        issue_ss_k(tdst, aK, q_addr(n));
         mma_commit(&bars->s_full);
       };
       auto issue_dp = [&](int n, uint32_t tdst) {
-        const uint32_t aDO = q_addr(n) + C::TILE;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSub + (kk & 3) * 32;
-          mma_ss(tdst, sw128_desc(aV + off, 16, 1024), sw128_desc(aDO + off, 16, 1024), idSS,
-                 kk > 0);
-        }
+        issue_ss_k(tdst, aV, q_addr(n) + C::TILE);
         mma_commit(&bars->dp_full);
       };
       bool ok = mbar_wait(&bars->kv_full, 0, abort_flag, p.err, p.wait_ns);
@@ -289,17 +296,40 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       tc_fence_after();
       if (ok) issue_dp(0, tb + 128);
       // tds: TMEM address of the region holding dS^T (bf16 pairs as the A operand).
-      auto issue_dk = [&](uint32_t aQ, int n, uint32_t tds) {
+      // A from TMEM (bf16 pairs at ta), B MN-major: dV += P^T dO, dK += dS^T Q.
+      auto issue_ts = [&](uint32_t tdst, uint32_t ta, uint32_t aB, bool acc) {
+        const uint64_t dB = sw128_desc(aB, kSub, 1024);
+        const uint32_t b_lo = static_cast<uint32_t>(dB);
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tb + C::COL_DK, tds + a_col(0, kk), sw128_desc(aQ + 2048 * kk, kSub, 1024),
-                 idKN, (n > 0 || kk > 0) ? 1u : 0u);
+        for (int g = 0; g < 2; ++g) {
+          uint32_t a4[4], db[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int kk = 4 * g + k;
+            a4[k] = ta + a_col(0, kk);
+            db[k] = b_lo + 128u * kk;
+          }
+          mma_ts_x4_lo(tdst, a4, db, static_cast<uint32_t>(dB >> 32), idKN,
+                       (acc || g > 0) ? 1u : 0u);
+        }
+      };
+      auto issue_dk = [&](uint32_t aQ, int n, uint32_t tds) {
+        issue_ts(tb + C::COL_DK, tds, aQ, n > 0);
       };
       auto issue_dq = [&](uint32_t tdst) {
+        const uint64_t dA = sw128_desc(aDS, kSub, 1024), dB = sw128_desc(aK, kSub, 1024);
+        const uint32_t a_lo = static_cast<uint32_t>(dA), b_lo = static_cast<uint32_t>(dB);
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ss(tdst, sw128_desc(aDS + 2048 * kk, kSub, 1024),
-                 sw128_desc(aK + 2048 * kk, kSub, 1024), idMN, kk > 0);
+        for (int g = 0; g < 2; ++g) {
+          uint32_t da[4], db[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            da[k] = a_lo + 128u * (4 * g + k);
+            db[k] = b_lo + 128u * (4 * g + k);
+          }
+          mma_ss_x4_lo(tdst, da, static_cast<uint32_t>(dA >> 32), db,
+                       static_cast<uint32_t>(dB >> 32), idMN, g > 0 ? 1u : 0u);
+        }
         mma_commit(&bars->dq_full);
       };
       int n = 0;
@@ -312,10 +342,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         ok = mbar_wait(&bars->p_ready, n & 1, abort_flag, p.err, p.wait_ns);
         tc_fence_after();
         if (!ok) break;
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tb + 256, tP + a_col(0, kk), sw128_desc(aDO + 2048 * kk, kSub, 1024), idKN,
-                 (n > 0 || kk > 0) ? 1u : 0u);
+        issue_ts(tb + 256, tP, aDO, n > 0);
         if constexpr (C::SEP_DQ) {
           if (in >= 0) {
             // S^T of the next block over P^T(n), which dV(n) (issued before it) reads first;

@@ -433,6 +433,43 @@ __device__ __forceinline__ void mma_ss_x4(uint32_t d_tmem, const uint64_t (&a)[4
 }
 
 // Four MMAs with A read from TMEM (addresses a[k]), B from shared memory.
+// Four MMAs whose descriptors differ only in their low 32 bits (the start address; stride,
+// version and swizzle sit in the high word): low words per MMA, one high word per operand.
+__device__ __forceinline__ void mma_ss_x4_lo(uint32_t d_tmem, const uint32_t (&a)[4], uint32_t a_hi,
+                                             const uint32_t (&b)[4], uint32_t b_hi, uint32_t idesc,
+                                             uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 a0, a1, a2, a3, b0, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %12, 0;\n\t"
+      "setp.ne.b32 t, %13, 0;\n\t"
+      "mov.b64 a0, {%2, %10};\n\tmov.b64 a1, {%3, %10};\n\tmov.b64 a2, {%4, %10};\n\tmov.b64 a3, {%5, %10};\n\t"
+      "mov.b64 b0, {%6, %11};\n\tmov.b64 b1, {%7, %11};\n\tmov.b64 b2, {%8, %11};\n\tmov.b64 b3, {%9, %11};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a0, b0, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %1, t;\n\t}" ::"r"(d_tmem), "r"(idesc),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]),
+      "r"(a_hi), "r"(b_hi), "r"(acc0), "r"(1u)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_x4_lo(uint32_t d_tmem, const uint32_t (&a)[4],
+                                             const uint32_t (&b)[4], uint32_t b_hi, uint32_t idesc,
+                                             uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 b0, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %11, 0;\n\t"
+      "setp.ne.b32 t, %12, 0;\n\t"
+      "mov.b64 b0, {%6, %10};\n\tmov.b64 b1, {%7, %10};\n\tmov.b64 b2, {%8, %10};\n\tmov.b64 b3, {%9, %10};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], b0, %1, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], b1, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], b2, %1, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], b3, %1, t;\n\t}" ::"r"(d_tmem), "r"(idesc),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]),
+      "r"(b_hi), "r"(acc0), "r"(1u)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, const uint32_t (&a)[4],
                                           const uint64_t (&b)[4], uint32_t idesc, uint32_t acc0) {
   asm volatile(
