@@ -156,8 +156,22 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   u.nb = (p.N + kBlk - 1) / kBlk;
   u.nq = u.nb;
   const int bhs = p.B * p.H;
-  u.bh = blockIdx.x % bhs;
-  u.j = blockIdx.x / bhs;           // key block; small j first (most query blocks under causal)
+  {
+    // Grid order: groups of G heads, G as large as keeps a group's Q and dO (bf16) and its dQ
+    // accumulator (fp32), 8 N d bytes per head, within 64 MiB of L2; in each group key block
+    // j ascending (small j first: the most query blocks under causal), the group's heads
+    // fastest.  The co-resident CTAs then read each Q and dO tile from DRAM about once and
+    // reduce into accumulators that stay in L2.  The dropout instance keeps all heads in one
+    // group (heads fastest), which measured faster for it.
+    const long long per_head = 8ll * p.N * D;
+    const int G = DROP ? bhs
+                       : static_cast<int>(max(1ll, min(static_cast<long long>(bhs),
+                                                       (64ll << 20) / per_head)));
+    const int b = blockIdx.x, g = b / (G * u.nb), r = b - g * G * u.nb;
+    const int Gg = min(G, bhs - g * G);
+    u.j = r / Gg;
+    u.bh = g * G + r % Gg;
+  }
 
   if (tid == 0) {
     mbar_init(&bars->kv_full, 1);
