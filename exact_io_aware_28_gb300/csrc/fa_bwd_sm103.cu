@@ -163,14 +163,18 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     // fastest.  The co-resident CTAs then read each Q and dO tile from DRAM about once and
     // reduce into accumulators that stay in L2.  The dropout instance keeps all heads in one
     // group (heads fastest), which measured faster for it.
-    const long long per_head = 8ll * p.N * D;
-    const int G = DROP ? bhs
-                       : static_cast<int>(max(1ll, min(static_cast<long long>(bhs),
-                                                       (64ll << 20) / per_head)));
-    const int b = blockIdx.x, g = b / (G * u.nb), r = b - g * G * u.nb;
-    const int Gg = min(G, bhs - g * G);
-    u.j = r / Gg;
-    u.bh = g * G + r % Gg;
+    if constexpr (DROP) {
+      u.bh = blockIdx.x % bhs;
+      u.j = blockIdx.x / bhs;
+    } else {
+      const long long per_head = 8ll * p.N * D;
+      const int G = static_cast<int>(
+          max(1ll, min(static_cast<long long>(bhs), (64ll << 20) / per_head)));
+      const int b = blockIdx.x, g = b / (G * u.nb), r = b - g * G * u.nb;
+      const int Gg = min(G, bhs - g * G);
+      u.j = r / Gg;
+      u.bh = g * G + r % Gg;
+    }
   }
 
   if (tid == 0) {
