@@ -17,11 +17,12 @@
 //                 read from TMEM; issue order PV0(j), S0(j+1), PV1(j), S1(j+1) keeps the
 //                 tensor pipe busy while each softmax warpgroup works on its own tile;
 //   warp 2        tensor-memory allocation;
-//   warps 4-7     softmax for tile 0, warps 8-11 softmax for tile 1: one thread per row,
-//                 scores read with tcgen05.ld, exp2 with scale*log2(e) folded in, P written
-//                 back as bf16 over the first 64 columns of its own S region, O rescaled in
-//                 TMEM only when the running maximum grows by more than 2^8 (exact: the
-//                 final division uses the same reference maximum);
+//   warps 4-11    softmax: all eight warps work on each tile in turn (tile 0, then tile 1,
+//                 for every key block), a thread holding two rows of 32 keys through the
+//                 16-lane TMEM shapes; scores read with tcgen05.ld, exp2 with scale*log2(e)
+//                 folded in, P written back as bf16 over the first 64 columns of the tile's S
+//                 region, O rescaled in TMEM only when the running maximum grows by more than
+//                 2^8 (exact: the final division uses the same reference maximum);
 //   epilogue      the softmax warps read O from TMEM, divide by the row sum and store bf16.
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [384,384+d).
 // Every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT and exits cleanly.
@@ -294,6 +295,15 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     float m_run[2][2] = {{-INFINITY, -INFINITY}, {-INFINITY, -INFINITY}};  // [tile][A/B]
     float l_part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
     int n_t[2] = {0, 0};
+    // Dropout: the generator's counter word x1 (this thread's row pair) is fixed per tile.
+    philox::PrefixX0 pfx[2] = {};
+    if constexpr (DROP) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        pfx[t] = philox::prefix_x0(philox::row_pair(u.q0 + t * kBlk + rA),
+                                   static_cast<uint32_t>(u.bh), p.drop_offset, p.drop_seed_lo,
+                                   p.drop_seed_hi);
+    }
     bool ok = true;
     for (int j = 0; j < jend && ok; ++j) {
 #pragma unroll
@@ -357,10 +367,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             // One generator call per four key chunks: word cc % 4 holds the bytes of keys
             // 8cc + 2(t % 4) + {0, 1} of rows A and B, in that order.
             if ((cc & 3) == 0) {
-              keep = philox::philox4x32_10(
-                  static_cast<uint32_t>(4 * (4 * j + (cc >> 2)) + t4),
-                  philox::row_pair(u.q0 + t * kBlk + rA), static_cast<uint32_t>(u.bh),
-                  p.drop_offset, p.drop_seed_lo, p.drop_seed_hi);
+              keep = philox::run_x0(pfx[t], static_cast<uint32_t>(4 * (4 * j + (cc >> 2)) + t4));
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 keep.w[k] = philox::keep_bytes(keep.w[k], 0x01010101u * p.drop_threshold);

@@ -30,20 +30,31 @@
 namespace fa {
 namespace philox {
 
+// High 32 bits of a 32 x 32-bit product: __umulhi on the device, the same value on the host
+// (the generator functions below also compile as host code, for the CPU tests).
+__host__ __device__ __forceinline__ uint32_t mulhi32(uint32_t a, uint32_t b) {
+#ifdef __CUDA_ARCH__
+  return __umulhi(a, b);
+#else
+  return static_cast<uint32_t>((static_cast<uint64_t>(a) * b) >> 32);
+#endif
+}
+
 struct Words {
   uint32_t w[4];
 };
 
-__device__ __forceinline__ Words philox4x32_10(uint32_t x0, uint32_t x1, uint32_t x2,
-                                               uint32_t x3, uint32_t k0, uint32_t k1) {
+__host__ __device__ __forceinline__ Words philox4x32_10(uint32_t x0, uint32_t x1,
+                                                        uint32_t x2, uint32_t x3,
+                                                        uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     if (r > 0) {
       k0 += 0x9E3779B9u;
       k1 += 0xBB67AE85u;
     }
-    const uint32_t hi0 = __umulhi(0xD2511F53u, x0), lo0 = 0xD2511F53u * x0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, x2), lo1 = 0xCD9E8D57u * x2;
+    const uint32_t hi0 = mulhi32(0xD2511F53u, x0), lo0 = 0xD2511F53u * x0;
+    const uint32_t hi1 = mulhi32(0xCD9E8D57u, x2), lo1 = 0xCD9E8D57u * x2;
     x0 = hi1 ^ x1 ^ k0;
     x1 = lo1;
     x2 = hi0 ^ x3 ^ k1;
@@ -52,11 +63,59 @@ __device__ __forceinline__ Words philox4x32_10(uint32_t x0, uint32_t x1, uint32_
   return Words{{x0, x1, x2, x3}};
 }
 
-__device__ __forceinline__ uint32_t row_pair(int i) {
+// The same generator for a stream of calls in which only x0 changes (x1, x2, x3 and the key
+// fixed): the 4 multiplies of rounds 1-2 that depend on the fixed words alone are formed once.
+struct PrefixX0 {
+  uint32_t x3k1;  // round 1: x3 ^ k1
+  uint32_t c1;    // round 1: x1'
+  uint32_t h0;    // round 2: high product of x0'
+  uint32_t l0;    // round 2: low product of x0'
+  uint32_t k0, k1;
+};
+
+__host__ __device__ __forceinline__ PrefixX0 prefix_x0(uint32_t x1, uint32_t x2,
+                                                        uint32_t x3, uint32_t k0,
+                                                        uint32_t k1) {
+  PrefixX0 s;
+  s.k0 = k0;
+  s.k1 = k1;
+  s.x3k1 = x3 ^ k1;
+  s.c1 = 0xCD9E8D57u * x2;
+  const uint32_t c0 = mulhi32(0xCD9E8D57u, x2) ^ x1 ^ k0;   // round 1: x0'
+  s.h0 = mulhi32(0xD2511F53u, c0);
+  s.l0 = 0xD2511F53u * c0;
+  return s;
+}
+
+__host__ __device__ __forceinline__ Words run_x0(const PrefixX0& s, uint32_t x0) {
+  // round 1
+  const uint32_t y2 = mulhi32(0xD2511F53u, x0) ^ s.x3k1;
+  const uint32_t y3 = 0xD2511F53u * x0;
+  // round 2
+  uint32_t k0 = s.k0 + 0x9E3779B9u, k1 = s.k1 + 0xBB67AE85u;
+  uint32_t z0 = mulhi32(0xCD9E8D57u, y2) ^ s.c1 ^ k0;
+  uint32_t z1 = 0xCD9E8D57u * y2;
+  uint32_t z2 = s.h0 ^ y3 ^ k1;
+  uint32_t z3 = s.l0;
+#pragma unroll
+  for (int r = 2; r < 10; ++r) {
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+    const uint32_t hi0 = mulhi32(0xD2511F53u, z0), lo0 = 0xD2511F53u * z0;
+    const uint32_t hi1 = mulhi32(0xCD9E8D57u, z2), lo1 = 0xCD9E8D57u * z2;
+    z0 = hi1 ^ z1 ^ k0;
+    z1 = lo1;
+    z2 = hi0 ^ z3 ^ k1;
+    z3 = lo0;
+  }
+  return Words{{z0, z1, z2, z3}};
+}
+
+__host__ __device__ __forceinline__ uint32_t row_pair(int i) {
   return static_cast<uint32_t>(8 * (i >> 4) + (i & 7));
 }
 
-__device__ __forceinline__ uint32_t key_octet(int j) {
+__host__ __device__ __forceinline__ uint32_t key_octet(int j) {
   return static_cast<uint32_t>(4 * (j >> 5) + ((j >> 1) & 3));
 }
 
