@@ -102,6 +102,20 @@ def test_named_workload_sampled_heads(name, heads):
 
 
 @pytest.mark.slow
+def test_grouped_grid_order_with_a_ragged_last_group():
+    # Both tensor-core kernels order their grids by groups of heads sized to L2 (at N = 16384,
+    # d = 128: eight heads per forward group, four per backward group).  Nine heads leave a
+    # last group of one head in both; that head and one from a full group against the oracle.
+    x = _inputs(1, 9, 16384, 128, "bf16", {"causal": True}, seed=23)
+    out = run_library(x)
+    heads = [(0, 3), (0, 8)]
+    errs = compare(out, run_oracle(x, heads=heads), "bf16", heads=heads)
+    print(errs)
+    for t in out:
+        assert torch.isfinite(t.float()).all() or t is out[1]
+
+
+@pytest.mark.slow
 def test_long_sequence_sampled_rows_and_gradient_sums():
     # N = 2^16 + 77 (a ragged tail at a size far past the bench's), causal, d = 128: sampled
     # rows of O and lse against the oracle, one row at a time; the gradients through the
