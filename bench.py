@@ -265,19 +265,24 @@ def summarize(ms):
     return out
 
 
-def pipelined_e2e(steps, host_in, dev_in, dev_out, host_out, compute, comp_stream):
+def pipelined_e2e(steps, host_in, dev_in, dev_out, host_out, compute, comp_stream, rates=None):
     """End-to-end time per step with the copies inside the timed region.
 
     Every step copies its inputs from pinned host memory (``host_in``) to the device and its
     results back to pinned host memory (``host_out``).  Two device buffer sets
     (``dev_in[0|1]``, ``dev_out[0|1]``) let step i+1's inputs travel on one copy stream and
     step i-1's results on another while step i computes, as a pipelined caller would run it.
-    ``compute(inputs, outputs)`` launches one step on ``comp_stream``.  Returns ms per step.
+    ``compute(inputs, outputs)`` launches one step on ``comp_stream``.  Returns ms per step;
+    if ``rates`` is a dict, it also gets the median time of one step's input copies
+    (``h2d_ms``) and of its result copies (``d2h_ms``), each timed on its copy stream.
     """
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
-    in_ready = [torch.cuda.Event() for _ in range(steps)]
+    timed = rates is not None
+    in_ready = [torch.cuda.Event(enable_timing=timed) for _ in range(steps)]
     done = [torch.cuda.Event() for _ in range(steps)]
-    copied = [torch.cuda.Event() for _ in range(steps)]
+    copied = [torch.cuda.Event(enable_timing=timed) for _ in range(steps)]
+    h_beg = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if timed else None
+    d_beg = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if timed else None
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -287,6 +292,8 @@ def pipelined_e2e(steps, host_in, dev_in, dev_out, host_out, compute, comp_strea
         with torch.cuda.stream(h2d_s):
             if i >= 2:
                 h2d_s.wait_event(done[i - 2])  # buffer set k is free again
+            if timed:
+                h_beg[i].record(h2d_s)
             for hsrc, ddst in zip(host_in, dev_in[k]):
                 ddst.copy_(hsrc, non_blocking=True)
             in_ready[i].record(h2d_s)
@@ -297,12 +304,19 @@ def pipelined_e2e(steps, host_in, dev_in, dev_out, host_out, compute, comp_strea
         done[i].record(comp_stream)
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(done[i])
+            if timed:
+                d_beg[i].record(d2h_s)
             for hdst, dsrc in zip(host_out, dev_out[k]):
                 hdst.copy_(dsrc, non_blocking=True)
             copied[i].record(d2h_s)
     d2h_s.wait_event(copied[steps - 1])
     t1.record(d2h_s)
     torch.cuda.synchronize()
+    if timed:
+        rates["h2d_ms"] = float(np.median([h_beg[i].elapsed_time(in_ready[i])
+                                           for i in range(steps)]))
+        rates["d2h_ms"] = float(np.median([d_beg[i].elapsed_time(copied[i])
+                                           for i in range(steps)]))
     return t0.elapsed_time(t1) / steps
 
 
@@ -611,14 +625,21 @@ def run_ours(args, world, rank, local):
     e2e_steps = max(2, min(args.steps, 20))
     dev_in = [(x.q, x.k, x.v, x.do), tuple(torch.empty_like(t) for t in (x.q, x.k, x.v, x.do))]
     dev_out = [(o, lse, dq, dk, dv), tuple(torch.empty_like(t) for t in (o, lse, dq, dk, dv))]
+    rates = {}
     e2e_ms = max_over_ranks(pipelined_e2e(e2e_steps, pin, dev_in, dev_out, outs, r["compute"],
-                                          r["stream"]), world)
+                                          r["stream"], rates), world)
     del dev_in, dev_out
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs)
+    # The host link's rates as these copies saw them (both directions at once, beside the
+    # compute): when one step's copies take longer than its compute, the e2e figure is the
+    # link's, not the kernels'.
     e2e = {"value": world * fl["fwd_bwd"] / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "steps": e2e_steps, "copies": "pipelined: step i+1 in and step i-1 out during step i"}
+           "steps": e2e_steps, "copies": "pipelined: step i+1 in and step i-1 out during step i",
+           "h2d_ms": rates["h2d_ms"], "d2h_ms": rates["d2h_ms"],
+           "h2d_gbs": h2d / (rates["h2d_ms"] * 1e-3) / 1e9,
+           "d2h_gbs": d2h / (rates["d2h_ms"] * 1e-3) / 1e9}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
