@@ -67,6 +67,9 @@ constexpr int kThreads = 512;
 constexpr int kRegsDrain = 168;    // warps 0-3
 constexpr int kRegsSoftmax = 136;  // warps 4-11
 constexpr int kRegsControl = 72;   // warps 12-15
+constexpr int kRegsLaunch = 128;   // 65536 / kThreads
+static_assert(4 * 32 * (kRegsDrain + 2 * kRegsSoftmax + kRegsControl) == kThreads * kRegsLaunch,
+              "register split must equal the launch allocation");
 
 template <int D>
 struct Cfg {
@@ -754,6 +757,15 @@ cudaError_t bwd_launch(const Problem& p, const void* q, const void* k, const voi
     cudaError_t e = cudaFuncSetAttribute(bwd_sm103_kernel<D, DROP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
     if (e != cudaSuccess) return e;
+    if constexpr (D == 128) {
+      // The in-kernel register split (drain, softmax, control) adds up to exactly 128 per
+      // thread at launch: a kernel built with another count would wait forever in
+      // setmaxnreg, so it is refused here.
+      cudaFuncAttributes fattr;
+      e = cudaFuncGetAttributes(&fattr, bwd_sm103_kernel<D, DROP>);
+      if (e != cudaSuccess) return e;
+      if (fattr.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+    }
     attr_set[dev].store(true);
   }
   const int nkb = (p.N + kBlk - 1) / kBlk;
