@@ -70,6 +70,10 @@ constexpr int kRegsControl = 72;   // warps 12-15
 constexpr int kRegsLaunch = 128;   // 65536 / kThreads
 static_assert(4 * 32 * (kRegsDrain + 2 * kRegsSoftmax + kRegsControl) == kThreads * kRegsLaunch,
               "register split must equal the launch allocation");
+// setmaxnreg.inc may only raise a warp's count and .dec only lower it.
+static_assert(kRegsDrain >= kRegsLaunch && kRegsSoftmax >= kRegsLaunch &&
+                  kRegsControl <= kRegsLaunch,
+              "drain and softmax warps take registers, control warps release them");
 
 template <int D>
 struct Cfg {
