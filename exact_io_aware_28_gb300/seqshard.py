@@ -23,7 +23,9 @@ tensors.  The move is a ring shift (send to rank r + 1, receive from rank r - 1)
 step's computation when the tensors are not changed by it (the key/value chunk) so that
 the transfer overlaps the kernels.  The same per-rank schedule also runs with every rank
 in one process (``chunked_forward`` / ``chunked_backward``), the ring shift then being a
-rotation of Python lists; that form splits a long sequence into chunks on one GPU.
+rotation of Python lists; that form splits a long sequence into chunks on one GPU, each
+emulated rank's kernels on a CUDA stream of its own (events order the hand-offs), so that
+the launches of one rank fill the tails of another's.
 
 Supported: bf16 or fp32 [B, H, n, d] chunks of equal length n, d in {64, 128}, dense or
 causal attention (top-left aligned over the whole sequence).  Key padding and block masks
@@ -178,38 +180,89 @@ def _run_distributed(gen, group):
             value = recv
 
 
-def _run_emulated(gens: List):
-    """Drive every rank's schedule in one process; a ring shift is a list rotation."""
+def _run_emulated(gens: List, streams=None):
+    """Drive every rank's schedule in one process; a ring shift is a list rotation.
+
+    With ``streams`` (one CUDA stream per rank) each rank's kernels go to its own stream, so
+    that one rank's launches fill the tails of another's: a posted tensor carries an event
+    recorded on the poster's stream, which the receiving rank's stream waits for, and it is
+    marked as used on the receiving stream for the caching allocator.  The caller's stream
+    waits for every rank's stream before the results are returned."""
     world = len(gens)
     results = [None] * world
     values = [None] * world
     posted = [dict() for _ in range(world)]
     live = list(range(world))
+    caller = torch.cuda.current_stream() if streams is not None else None
+    if streams is not None:
+        for st in streams:
+            st.wait_stream(caller)          # the inputs were written on the caller's stream
+
+    def on(r):
+        return torch.cuda.stream(streams[r]) if streams is not None else _nullctx()
+
     while live:
         waiting = {}
         for r in live:
-            while True:
-                try:
-                    msg = gens[r].send(values[r])
-                except StopIteration as stop:
-                    results[r] = stop.value
-                    break
-                values[r] = None
-                if msg[0] == "post":
-                    posted[r][msg[1]] = msg[2]
-                else:
-                    waiting[r] = msg[1]
-                    break
+            with on(r):
+                while True:
+                    try:
+                        msg = gens[r].send(values[r])
+                    except StopIteration as stop:
+                        results[r] = stop.value
+                        break
+                    values[r] = None
+                    if msg[0] == "post":
+                        ev = None
+                        if streams is not None:
+                            ev = torch.cuda.Event()
+                            ev.record(streams[r])
+                        posted[r][msg[1]] = (msg[2], ev)
+                    else:
+                        waiting[r] = msg[1]
+                        break
         done = [r for r in live if results[r] is not None]
         live = [r for r in live if results[r] is None]
         if live and done:
             raise RuntimeError("ranks finished out of step")
         for r in live:
-            tag = waiting[r]
-            values[r] = posted[(r - 1) % world][tag]
+            tensors, ev = posted[(r - 1) % world][waiting[r]]
+            if streams is not None:
+                streams[r].wait_event(ev)
+                for t in tensors:
+                    t.record_stream(streams[r])
+            values[r] = tensors
         for r in live:
             posted[(r - 1) % world].pop(waiting[r], None)
+    if streams is not None:
+        for r, st in enumerate(streams):
+            caller.wait_stream(st)
+            for t in _tensors_of(results[r]):
+                t.record_stream(caller)
     return results
+
+
+class _nullctx:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *exc):
+        return False
+
+
+def _tensors_of(x):
+    if isinstance(x, torch.Tensor):
+        return [x]
+    if isinstance(x, (tuple, list)):
+        return [t for y in x for t in _tensors_of(y)]
+    return []
+
+
+def _rank_streams(t: torch.Tensor, world: int):
+    """One stream per emulated rank for CUDA tensors, none on the CPU."""
+    if t.device.type != "cuda":
+        return None
+    return [torch.cuda.Stream(device=t.device) for _ in range(world)]
 
 
 def _check(chunks: Sequence[torch.Tensor]):
@@ -251,7 +304,7 @@ def chunked_forward(qs, ks, vs, causal: bool = False, scale: Optional[float] = N
     ops = ops or CudaShardOps()
     W = len(qs)
     return _run_emulated([_forward_schedule(ops, r, W, qs[r], ks[r], vs[r], causal, scale)
-                          for r in range(W)])
+                          for r in range(W)], _rank_streams(qs[0], W))
 
 
 def chunked_backward(qs, ks, vs, os_, lses, dos, causal: bool = False,
@@ -262,4 +315,5 @@ def chunked_backward(qs, ks, vs, os_, lses, dos, causal: bool = False,
     ops = ops or CudaShardOps()
     W = len(qs)
     return _run_emulated([_backward_schedule(ops, r, W, qs[r], ks[r], vs[r], os_[r], lses[r],
-                                             dos[r], causal, scale) for r in range(W)])
+                                             dos[r], causal, scale) for r in range(W)],
+                         _rank_streams(qs[0], W))
