@@ -36,7 +36,9 @@
  * Errors: arguments are validated on the host before any launch; a failed check returns
  * FA_ERR_INVALID_ARG (bad pointer, size, alignment, dtype, workspace) or FA_ERR_UNSUPPORTED
  * (a shape the kernels do not cover) and launches nothing.  A launch failure reported by the
- * CUDA runtime returns FA_ERR_CUDA.  Device-side faults surface at the caller's next
+ * CUDA runtime returns FA_ERR_CUDA; so does a tensor-core kernel that was built with another
+ * register count than its in-kernel register split assumes (the first call on a device
+ * checks it and then launches nothing).  Device-side faults surface at the caller's next
  * synchronisation.  A bounded wait inside a kernel that runs out records FA_ERR_TIMEOUT in
  * the library's device error word, readable with fa_device_error().
  */
